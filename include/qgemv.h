@@ -1,0 +1,167 @@
+/*
+ * qgemv.h - C ABI of the quantized-weight GEMV library for NVIDIA GB300 (sm_103a).
+ *
+ * The library computes the decode-time matrix-vector product against
+ * block-quantised weights: y = W_deq x with the activation x quantised to int8
+ * per block of 32 and the weights stored as 4-bit or 6-bit codes with an fp16
+ * scale and min per block of 32 (w = scale * code + min).  Its neighbours are a
+ * small-batch variant, a Walsh-Hadamard + codebook (CQ) matvec, and a
+ * vocabulary projection finished with logit soft-capping and argmax.
+ *
+ * Conventions for every call:
+ *  - Pointers named as device buffers are CUDA device pointers owned by the
+ *    caller; the library keeps no reference to them after the call returns.
+ *  - Calls are asynchronous: arguments are validated on the host, the work is
+ *    enqueued on `stream` (a cudaStream_t passed as void*; NULL is the legacy
+ *    default stream) and the call returns without synchronising.
+ *  - A negative return value is an error; nothing was enqueued and no output
+ *    was touched.  QG_ERR_CUDA reports a launch failure seen right after the
+ *    launch; faults raised while a kernel runs surface at the caller's next
+ *    synchronisation, like any CUDA error.
+ *  - The library allocates no device memory.  Calls are thread-safe.
+ *
+ * Weight layout (blocks of 32 consecutive weights along K; rows row-major):
+ *  Q4  codes  uint8 [n][k/2]: byte 16*b + j of a row holds code 32*b + j in
+ *             bits 0-3 and code 32*b + j + 16 in bits 4-7.
+ *  Q6  lo     uint8 [n][k/2]: the low 4 bits of each code, in the Q4 order;
+ *      hi     uint8 [n][k/4]: 8 bytes per block, byte 8*b + t holding the top
+ *             2 bits of codes 32*b + t, +8, +16, +24 in bits 0-1, 2-3, 4-5, 6-7.
+ *  scale, min binary16 (as uint16 bits) [n][k/32]; weight = scale*code + min.
+ *  CQ  idx    uint8 [n][k/2]: index 2j in bits 0-3 of byte j, 2j+1 in bits 4-7;
+ *      codebook binary16 [16]; row_scale binary16 [n].
+ * Packed planes, x and y must start on 16-byte boundaries.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum qg_status {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = -1, /* null pointer, size out of range, k not a multiple of 32, ... */
+    QG_ERR_ALIGNMENT = -2,   /* a buffer that must start on a 16-byte boundary does not */
+    QG_ERR_UNSUPPORTED = -3, /* bits other than 4/6, group size not supported, shape too large */
+    QG_ERR_WORKSPACE = -4,   /* workspace missing or smaller than the reported size */
+    QG_ERR_CUDA = -5         /* the CUDA launch itself failed */
+};
+
+/* Launch flags (bitwise OR; 0 = defaults). */
+#define QG_FLAG_PDL 0x1u    /* programmatic dependent launch: the kernel may start, and      \
+                               begin streaming WEIGHTS, before the preceding work on the     \
+                               stream has finished; it waits for that work before reading x, \
+                               writing any output or touching the workspace.  The caller     \
+                               guarantees that no preceding work writes the weights.         */
+#define QG_FLAG_PLAIN 0x2u  /* force the plain-load kernel (128-bit loads, no bulk-copy ring) */
+
+/* Largest supported sizes. */
+#define QG_MAX_K 65536       /* qgemv_q4/q6 and vocab: k <= QG_MAX_K */
+#define QG_MAX_BATCH 16      /* qgemv_batched: 1 <= batch <= 16 */
+#define QG_MAX_CQ_K 16384    /* cq_fwht_matvec: k <= QG_MAX_CQ_K */
+
+/* Human-readable text of a status code (static storage). */
+const char* qg_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int qg_version(void);
+
+/*
+ * Device-side error word.  Kernels that wait on an mbarrier give up after a
+ * bounded time and record a nonzero code here instead of hanging.  Reads and
+ * clears the word of the current device; synchronises the device.
+ * Returns QG_OK or QG_ERR_CUDA; *code receives the word (0 = no error).
+ */
+int qg_device_error(uint32_t* code);
+
+/*
+ * qgemv_q4: y[r] = sum_i (scale*code(r,i) + min) * x_deq(i),  r < n.
+ * x_deq is x quantised per block of 32: s_b = max|x| / 127 (fp32),
+ * xq = clamp(rint(x / s_b), -127, 127), x_deq = s_b * xq.  The integer block
+ * dots sum(code * xq) are exact; the block combine and row sum are fp32.
+ * Dequant-fused GEMV over int8 dp4a block dots (genie-ai-runtime v1.1 -> v1.3.1,
+ * "The decode arc": dp4a int8 MMVQ; oxinfer README, "How it works": per-matmul
+ * activation quantisation and int8 block dots).
+ *   codes, scale, min : device, Q4 layout above, n x k
+ *   n >= 0, k > 0, k % 32 == 0, k <= QG_MAX_K
+ *   x : device fp32 [k];  y : device fp32 [n] (written)
+ * n == 0 enqueues nothing and returns QG_OK.
+ */
+int qgemv_q4(const uint8_t* codes, const uint16_t* scale, const uint16_t* min, int n, int k, const float* x,
+             float* y, unsigned flags, void* stream);
+
+/* qgemv_q6: as qgemv_q4 with 6-bit codes (lo, hi planes). */
+int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n, int k,
+             const float* x, float* y, unsigned flags, void* stream);
+
+/*
+ * qgemv_batched: Y[c][r] = GEMV of column c, for c < batch: every activation
+ * column X[c] (fp32 [k], contiguous rows of X [batch][k]) is quantised on its
+ * own and all columns share one pass over the weights (the multi-token int8
+ * kernels of the oxinfer README, "Speculative decoding" and "How it works").
+ *   bits : 4 (hi must be NULL) or 6
+ *   1 <= batch <= QG_MAX_BATCH;  batch * k <= 131072
+ *   X : device fp32 [batch][k];  Y : device fp32 [batch][n] (written)
+ */
+int qgemv_batched(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n,
+                  int k, int batch, const float* X, float* Y, unsigned flags, void* stream);
+
+/*
+ * cq_fwht_matvec: selected-row codebook matvec in the Hadamard domain
+ * (needle.js "Inference backends": "Pure TypeScript" and "TypeGPU" for the
+ * normalised fast Walsh-Hadamard transform of each activation group followed by
+ * packed codebook-index decode inside the dot; "Custom backend" for the
+ * optional row range).
+ *   u = (1/sqrt(group)) * H_group x, independently for each group of `group`
+ *       consecutive values (H in natural / Sylvester order);
+ *   y[j] = row_scale[r] * sum_i codebook[idx(r, i)] * u[i],  r = row_start + j.
+ *   idx : device [n][k/2];  codebook : device binary16 [16];  row_scale : device binary16 [n]
+ *   group in {128, 256, 512, 1024};  k % group == 0;  k <= QG_MAX_CQ_K
+ *   0 <= row_start, 0 <= row_count, row_start + row_count <= n
+ *   x : device fp32 [k];  y : device fp32 [row_count] (written)
+ */
+int cq_fwht_matvec(const uint8_t* idx, const uint16_t* codebook, const uint16_t* row_scale, int n, int k, int group,
+                   int row_start, int row_count, const float* x, float* y, unsigned flags, void* stream);
+
+/*
+ * Workspace bytes that vocab_softcap_argmax needs (a small, fixed amount).
+ * The workspace is device memory owned by the caller; it must be zero-filled
+ * once after allocation, and every completed call leaves it zeroed again.
+ * Calls that share one workspace must not overlap in time on the GPU.
+ */
+size_t qg_vocab_workspace_bytes(void);
+
+/*
+ * vocab_softcap_argmax: z = the GEMV of qgemv_q4/q6 over n_vocab rows, then
+ * logits l = softcap * tanh(z / softcap) (final-logit soft-capping of
+ * genie-ai-runtime, "What Gemma 4 E2B actually is"; softcap <= 0 leaves z
+ * as is), and the index of the largest logit, the lowest index among equal
+ * maxima and NaN never winning (the deterministic argmax of the Gemma WebGPU
+ * Engine, "Roadmap").
+ *   bits : 4 or 6;  logits : device fp32 [n_vocab] or NULL (not written);
+ *   argmax : device int32 [1] (written);  ws : see qg_vocab_workspace_bytes.
+ *   1 <= n_vocab
+ */
+int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
+                         int n_vocab, int k, const float* x, float softcap, float* logits, int32_t* argmax, void* ws,
+                         size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * Exposed steps, for exactness checks of the integer parts.
+ * qg_quantize_act: per-block int8 quantisation of `batch` rows of x [batch][k]:
+ *   xq int8 [batch][k], xs fp32 [batch][k/32] (s_b), xsum int32 [batch][k/32] (sum of xq).
+ * qg_blockdots: D[r][b] = sum_{i<32} code(r, 32b+i) * xq(32b+i), int32 [n][k/32].
+ * Same size rules as qgemv_q4; all pointers device.
+ */
+int qg_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, void* stream);
+int qg_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,
+                 void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,233 @@
+// C ABI of the library: argument validation, variant choice, launch.
+#include <mutex>
+
+#include "qg_internal.h"
+
+namespace qg {
+
+// Device error word (see qg_device_error); kernels get its address as a parameter.
+__device__ unsigned int g_error_word = 0u;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    unsigned int* err = nullptr;
+};
+DeviceInfo g_dev[MAX_DEVICES];
+std::mutex g_mu;
+
+// (kernel, device) pairs whose opt-in shared-memory limit was already raised
+struct AttrEntry {
+    const void* kernel;
+    int device;
+    size_t smem;
+};
+AttrEntry g_attr[512];
+int g_attr_n = 0;
+
+int resolve(void* stream, unsigned flags, LaunchCtx& lc) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        (void)cudaGetLastError();
+        return QG_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& di = g_dev[dev];
+    if (!di.ready) {
+        if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err), g_error_word) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return QG_ERR_CUDA;
+        }
+        di.ready = true;
+    }
+    lc.stream = reinterpret_cast<cudaStream_t>(stream);
+    lc.flags = flags;
+    lc.device = dev;
+    lc.sm_count = di.sm_count;
+    lc.max_smem_optin = di.max_smem_optin;
+    lc.err = di.err;
+    return QG_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int ensure_smem_attr(const void* kernel, size_t smem, const LaunchCtx& lc) {
+    if (smem <= 48 * 1024) return QG_OK;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_attr_n; ++i)
+        if (g_attr[i].kernel == kernel && g_attr[i].device == lc.device) return g_attr[i].smem >= smem ? QG_OK : QG_ERR_UNSUPPORTED;
+    // raise to the most the kernel can take beside its static shared memory, once, so
+    // that later calls with other sizes need no new call
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QG_ERR_CUDA;
+    }
+    const int maxdyn = lc.max_smem_optin - (int)fa.sharedSizeBytes;
+    if (maxdyn < (int)smem) return QG_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxdyn) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QG_ERR_CUDA;
+    }
+    if (g_attr_n < 512) g_attr[g_attr_n++] = AttrEntry{kernel, lc.device, (size_t)maxdyn};
+    return QG_OK;
+}
+
+static int check_weights(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
+                         int n, int k) {
+    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
+    if (n < 0 || k <= 0 || (k & 31) != 0 || k > QG_MAX_K) return QG_ERR_INVALID_ARG;
+    if (n == 0) return QG_OK;
+    if (!lo || !scale || !min || (bits == 6 && !hi) || (bits == 4 && hi)) return QG_ERR_INVALID_ARG;
+    if (!aligned16(lo) || (bits == 6 && !aligned16(hi)) || !aligned16(scale) || !aligned16(min))
+        return QG_ERR_ALIGNMENT;
+    return QG_OK;
+}
+
+static int gemv_common(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
+                       int n, int k, int batch, const float* x, float* y, unsigned flags, void* stream) {
+    int rc = check_weights(bits, lo, hi, scale, min, n, k);
+    if (rc != QG_OK) return rc;
+    if (batch < 1 || batch > QG_MAX_BATCH || (long long)batch * k > 131072) return QG_ERR_INVALID_ARG;
+    if (n == 0) return QG_OK;
+    if (!x || !y) return QG_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    rc = resolve(stream, flags, lc);
+    if (rc != QG_OK) return rc;
+    if (!(flags & QG_FLAG_PLAIN) && stream_supported(bits, n, k, batch, EPI_STORE)) {
+        StreamParams sp = {lo, hi, scale, min, n, k, batch, 0, 0, x, y, 0.0f, nullptr, nullptr, nullptr};
+        rc = launch_stream(sp, bits, EPI_STORE, lc);
+        if (rc != QG_ERR_UNSUPPORTED) return rc;
+    }
+    PlainParams pp = {lo, hi, scale, min, n, k, batch, x, y, 0.0f, nullptr, nullptr};
+    return launch_plain(pp, bits, EPI_STORE, lc);
+}
+
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+const char* qg_status_string(int status) {
+    switch (status) {
+        case QG_OK:
+            return "ok";
+        case QG_ERR_INVALID_ARG:
+            return "invalid argument";
+        case QG_ERR_ALIGNMENT:
+            return "buffer not 16-byte aligned";
+        case QG_ERR_UNSUPPORTED:
+            return "unsupported format or size";
+        case QG_ERR_WORKSPACE:
+            return "workspace missing or too small";
+        case QG_ERR_CUDA:
+            return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+int qg_version(void) { return 100; }
+
+int qg_device_error(uint32_t* code) {
+    if (!code) return QG_ERR_INVALID_ARG;
+    unsigned int v = 0, zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return QG_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return QG_ERR_CUDA;
+    *code = v;
+    return QG_OK;
+}
+
+int qgemv_q4(const uint8_t* codes, const uint16_t* scale, const uint16_t* min, int n, int k, const float* x,
+             float* y, unsigned flags, void* stream) {
+    return gemv_common(4, codes, nullptr, scale, min, n, k, 1, x, y, flags, stream);
+}
+
+int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n, int k,
+             const float* x, float* y, unsigned flags, void* stream) {
+    if (!hi && n > 0) return QG_ERR_INVALID_ARG;
+    return gemv_common(6, lo, hi, scale, min, n, k, 1, x, y, flags, stream);
+}
+
+int qgemv_batched(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n,
+                  int k, int batch, const float* X, float* Y, unsigned flags, void* stream) {
+    return gemv_common(bits, lo, hi, scale, min, n, k, batch, X, Y, flags, stream);
+}
+
+int cq_fwht_matvec(const uint8_t* idx, const uint16_t* codebook, const uint16_t* row_scale, int n, int k, int group,
+                   int row_start, int row_count, const float* x, float* y, unsigned flags, void* stream) {
+    if (group != 128 && group != 256 && group != 512 && group != 1024) return QG_ERR_UNSUPPORTED;
+    if (n < 0 || k <= 0 || k % group != 0 || k > QG_MAX_CQ_K) return QG_ERR_INVALID_ARG;
+    if (row_start < 0 || row_count < 0 || (long long)row_start + row_count > n) return QG_ERR_INVALID_ARG;
+    if (row_count == 0) return QG_OK;
+    if (!idx || !codebook || !row_scale || !x || !y) return QG_ERR_INVALID_ARG;
+    if (!aligned16(idx) || !aligned16(x) || !aligned16(y)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    int rc = resolve(stream, flags, lc);
+    if (rc != QG_OK) return rc;
+    CqParams p = {idx, codebook, row_scale, n, k, group, row_start, row_count,
+                  (float)(1.0 / sqrt((double)group)), x, y};
+    return launch_cq(p, lc);
+}
+
+size_t qg_vocab_workspace_bytes(void) { return sizeof(VocabWorkspace); }
+
+int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
+                         int n_vocab, int k, const float* x, float softcap, float* logits, int32_t* argmax, void* ws,
+                         size_t ws_bytes, unsigned flags, void* stream) {
+    int rc = check_weights(bits, lo, hi, scale, min, n_vocab, k);
+    if (rc != QG_OK) return rc;
+    if (n_vocab < 1) return QG_ERR_INVALID_ARG;
+    if (!x || !argmax) return QG_ERR_INVALID_ARG;
+    if (!(softcap == softcap)) return QG_ERR_INVALID_ARG;  // NaN cap
+    if (!aligned16(x) || (logits && !aligned16(logits))) return QG_ERR_ALIGNMENT;
+    if (!ws || ws_bytes < sizeof(VocabWorkspace)) return QG_ERR_WORKSPACE;
+    if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    rc = resolve(stream, flags, lc);
+    if (rc != QG_OK) return rc;
+    VocabWorkspace* w = reinterpret_cast<VocabWorkspace*>(ws);
+    if (!(flags & QG_FLAG_PLAIN) && stream_supported(bits, n_vocab, k, 1, EPI_ARGMAX)) {
+        StreamParams sp = {lo, hi, scale, min, n_vocab, k, 1, 0, 0, x, logits, softcap, argmax, w, nullptr};
+        rc = launch_stream(sp, bits, EPI_ARGMAX, lc);
+        if (rc != QG_ERR_UNSUPPORTED) return rc;
+    }
+    PlainParams pp = {lo, hi, scale, min, n_vocab, k, 1, x, logits, softcap, argmax, w};
+    return launch_plain(pp, bits, EPI_ARGMAX, lc);
+}
+
+int qg_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, void* stream) {
+    if (k <= 0 || (k & 31) != 0 || k > QG_MAX_K || batch < 1 || batch > QG_MAX_BATCH) return QG_ERR_INVALID_ARG;
+    if (!x || !xq || !xs || !xsum) return QG_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    int rc = resolve(stream, 0, lc);
+    if (rc != QG_OK) return rc;
+    return launch_quantize_act(x, k, batch, xq, xs, xsum, lc);
+}
+
+int qg_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,
+                 void* stream) {
+    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
+    if (n < 0 || k <= 0 || (k & 31) != 0 || k > QG_MAX_K) return QG_ERR_INVALID_ARG;
+    if (n == 0) return QG_OK;
+    if (!lo || !xq || !dots || (bits == 6 && !hi) || (bits == 4 && hi)) return QG_ERR_INVALID_ARG;
+    if (!aligned16(lo) || (bits == 6 && !aligned16(hi)) || !aligned16(xq)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    int rc = resolve(stream, 0, lc);
+    if (rc != QG_OK) return rc;
+    return launch_blockdots(bits, lo, hi, n, k, xq, dots, lc);
+}
+
+}  // extern "C"

@@ -1,0 +1,141 @@
+// Codebook-quantised (CQ) matvec in the Hadamard domain.
+//
+// needle.js "Inference backends", "Pure TypeScript": the activation is first put
+// through a normalised fast Walsh-Hadamard transform per group, then the packed
+// 4-bit codebook indices are decoded inside the dot product, so the inverse
+// transform of the weights is never materialised.  "TypeGPU": one 32-lane group
+// per output row.  "Custom backend": an optional contiguous row range.
+//
+// Each CTA transforms x itself: a warp owns a group of G = 32*J values, lane l
+// holding elements J*l .. J*l+J-1.  The butterflies over the low log2(J) index
+// bits run in registers, those over the lane bits through __shfl_xor_sync.  The
+// result is kept in shared memory transposed (element J*l + j at j*32 + l), so
+// that in the dot loop lane l reads its J values without bank conflicts.
+#include "qg_internal.h"
+
+namespace qg {
+
+template <int J>
+__device__ __forceinline__ void load_lane_group(const float* __restrict__ src, float (&v)[J]) {
+    if constexpr (J % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < J / 4; ++q) {
+            const float4 t = reinterpret_cast<const float4*>(src)[q];
+            v[4 * q] = t.x;
+            v[4 * q + 1] = t.y;
+            v[4 * q + 2] = t.z;
+            v[4 * q + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j) v[j] = src[j];
+    }
+}
+
+// J/2 index bytes of one lane as 32-bit words (J/8 words; J = 4 uses the low half of one)
+template <int J>
+__device__ __forceinline__ void load_lane_indices(const uint8_t* __restrict__ src, uint32_t (&w)[(J + 7) / 8]) {
+    if constexpr (J == 32) {
+        const uint4 t = ldg_stream16(src);
+        w[0] = t.x;
+        w[1] = t.y;
+        w[2] = t.z;
+        w[3] = t.w;
+    } else if constexpr (J == 16) {
+        const uint2 t = ldg_stream8(src);
+        w[0] = t.x;
+        w[1] = t.y;
+    } else if constexpr (J == 8) {
+        w[0] = __ldg(reinterpret_cast<const unsigned int*>(src));
+    } else {
+        w[0] = ldg_stream2(src);
+    }
+}
+
+template <int J>
+__global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
+    constexpr int G = 32 * J;
+    extern __shared__ __align__(16) float su[];  // [k], transposed per group
+    __shared__ float scb[16];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int ngroups = p.k / G;
+
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    if (threadIdx.x < 16) scb[threadIdx.x] = half_bits_to_float(p.codebook[threadIdx.x]);
+
+    for (int g = wid; g < ngroups; g += 8) {
+        float v[J];
+        load_lane_group<J>(p.x + (size_t)g * G + J * lane, v);
+#pragma unroll
+        for (int h = 1; h < J; h <<= 1) {
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                if ((j & h) == 0) {
+                    const float a = v[j], b = v[j + h];
+                    v[j] = a + b;
+                    v[j + h] = a - b;
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[j], m);
+                v[j] = upper ? (o - v[j]) : (v[j] + o);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) su[g * G + j * 32 + lane] = v[j] * p.inv_sqrt_group;
+    }
+    __syncthreads();
+
+    const size_t row_bytes = (size_t)(p.k >> 1);
+    for (int j = blockIdx.x * 8 + wid; j < p.row_count; j += gridDim.x * 8) {
+        const int r = p.row_start + j;
+        const uint8_t* rp = p.idx + (size_t)r * row_bytes;
+        float acc = 0.0f;
+        for (int g = 0; g < ngroups; ++g) {
+            uint32_t w[(J + 7) / 8];
+            load_lane_indices<J>(rp + (size_t)g * (G / 2) + (J / 2) * lane, w);
+            const float* ug = su + g * G + lane;
+#pragma unroll
+            for (int e = 0; e < J; ++e) {
+                const uint32_t c = (w[e >> 3] >> (4 * (e & 7))) & 15u;
+                acc = fmaf(scb[c], ug[e * 32], acc);
+            }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) p.y[j] = half_bits_to_float(p.row_scale[r]) * acc;
+    }
+}
+
+template <int J>
+static int launch_cq_t(const CqParams& p, const LaunchCtx& lc) {
+    auto kern = cq_kernel<J>;
+    const size_t smem = (size_t)p.k * sizeof(float);
+    if (smem > (size_t)lc.max_smem_optin) return QG_ERR_UNSUPPORTED;
+    if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
+    int grid = (p.row_count + 7) / 8;
+    if (grid > lc.sm_count * 8) grid = lc.sm_count * 8;
+    if (grid < 1) grid = 1;
+    return launch_kernel(kern, dim3(grid), dim3(256), smem, lc, p);
+}
+
+int launch_cq(const CqParams& p, const LaunchCtx& lc) {
+    switch (p.group) {
+        case 128:
+            return launch_cq_t<4>(p, lc);
+        case 256:
+            return launch_cq_t<8>(p, lc);
+        case 512:
+            return launch_cq_t<16>(p, lc);
+        case 1024:
+            return launch_cq_t<32>(p, lc);
+    }
+    return QG_ERR_UNSUPPORTED;
+}
+
+}  // namespace qg

@@ -1,0 +1,178 @@
+// Plain-load quantized-weight GEMV kernels: any k % 32 == 0, any n.
+//
+// One warp per output row (the warp-per-row GEMV of genie-ai-runtime, "The decode
+// arc"; one 32-lane group per row in needle.js "Inference backends", "TypeGPU").
+// Lane l takes blocks l, l+32, ... of the row: each block is one 16-byte load of
+// codes (a whole Q4 block), decoded in registers and dotted with the int8
+// activation by dp4a (genie-ai-runtime, "The decode arc": dp4a int8 MMVQ
+// "instead of dequant-to-fp"; its 32-bit-word unpack of the Q4_K fast path).
+// Every CTA quantises the activation columns into shared memory first.
+#include "qg_internal.h"
+
+namespace qg {
+
+template <int BITS, int BC, int EPI>
+__global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int nb = p.k >> 5;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int xstride = xq_stride(nb);
+
+    pdl_wait();  // x, y and the workspace may belong to the preceding kernel
+    if (threadIdx.x == 0) pdl_launch_dependents();
+
+    for (int c = 0; c < p.batch; ++c)
+        quantize_to_smem(p.x + (size_t)c * p.k, nb, xq_view(smem + c * xstride, nb), wid, 8);
+    __syncthreads();
+
+    float bv = __int_as_float(0x7fc00000);
+    int bi = 0x7fffffff;
+    const size_t code_row = (size_t)(p.k >> 1), hi_row = (size_t)(p.k >> 2);
+
+    for (int r = blockIdx.x * 8 + wid; r < p.n; r += gridDim.x * 8) {
+        float acc[BC];
+#pragma unroll
+        for (int c = 0; c < BC; ++c) acc[c] = 0.0f;
+        const uint8_t* crow = p.lo + (size_t)r * code_row;
+        const uint8_t* hrow = (BITS == 6) ? p.hi + (size_t)r * hi_row : nullptr;
+        const uint16_t* srow = p.scale + (size_t)r * nb;
+        const uint16_t* mrow = p.min + (size_t)r * nb;
+#pragma unroll 2
+        for (int b = lane; b < nb; b += 32) {
+            const uint4 cw = ldg_stream16(crow + 16 * (size_t)b);
+            Codes32 cc;
+            if constexpr (BITS == 4)
+                cc = unpack_q4(cw);
+            else
+                cc = unpack_q6(cw, ldg_stream8(hrow + 8 * (size_t)b));
+            const float d = half_bits_to_float(ldg_stream2(srow + b));
+            const float m = half_bits_to_float(ldg_stream2(mrow + b));
+#pragma unroll
+            for (int c = 0; c < BC; ++c) {
+                if (c < p.batch) {
+                    const XqView v = xq_view(smem + c * xstride, nb);
+                    const uint4 xl = *reinterpret_cast<const uint4*>(v.lo + 16 * b);
+                    const uint4 xh = *reinterpret_cast<const uint4*>(v.hi + 16 * b);
+                    acc[c] += block_combine(block_dot(cc, xl, xh), d, m, v.s[b], v.S[b]);
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < BC; ++c) acc[c] = warp_sum(acc[c]);
+        if constexpr (EPI == EPI_STORE) {
+            if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < BC; ++c)
+                    if (c < p.batch) p.y[(size_t)c * p.n + r] = acc[c];
+            }
+        } else {
+            const float l = softcap_apply(acc[0], p.softcap);
+            if (lane == 0 && p.y) p.y[r] = l;
+            if (better(l, r, bv, bi)) {
+                bv = l;
+                bi = r;
+            }
+        }
+    }
+    if constexpr (EPI == EPI_ARGMAX) {
+        __shared__ ArgmaxPartial sred[8];
+        __shared__ int sflag;
+        argmax_finish(bv, bi, p.ws, p.argmax, sred, &sflag);
+    }
+}
+
+// Exposed step: per-block activation quantisation of `batch` rows of x, one warp per block.
+__global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ x, int k, int batch,
+                                                           int8_t* __restrict__ xq, float* __restrict__ xs,
+                                                           int32_t* __restrict__ xsum) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const long long total = (long long)batch * (k >> 5);
+    for (long long blk = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); blk < total;
+         blk += (long long)gridDim.x * 8) {
+        float s;
+        int S;
+        const int q = quantize_lane(x[blk * 32 + lane], s, S);
+        xq[blk * 32 + lane] = (int8_t)q;
+        if (lane == 0) {
+            xs[blk] = s;
+            xsum[blk] = S;
+        }
+    }
+}
+
+// Exposed step: integer block dots D[r][b], one thread per (row, block).
+template <int BITS>
+__global__ void __launch_bounds__(256) blockdots_kernel(const uint8_t* __restrict__ lo, const uint8_t* __restrict__ hi,
+                                                        int n, int k, const int8_t* __restrict__ xq,
+                                                        int32_t* __restrict__ dots) {
+    pdl_wait();
+    const int nb = k >> 5;
+    const long long total = (long long)n * nb;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long r = t / nb;
+        const int b = (int)(t - r * nb);
+        const uint4 cw = ldg_stream16(lo + r * (k >> 1) + 16 * b);
+        Codes32 cc;
+        if constexpr (BITS == 4)
+            cc = unpack_q4(cw);
+        else
+            cc = unpack_q6(cw, ldg_stream8(hi + r * (k >> 2) + 8 * b));
+        const uint4 xl = *reinterpret_cast<const uint4*>(xq + 32 * b);
+        const uint4 xh = *reinterpret_cast<const uint4*>(xq + 32 * b + 16);
+        dots[t] = block_dot(cc, xl, xh);
+    }
+}
+
+// ---------------------------------------------------------------- host launchers
+template <int BITS, int BC, int EPI>
+static int launch_plain_t(const PlainParams& p, const LaunchCtx& lc) {
+    auto kern = gemv_plain_kernel<BITS, BC, EPI>;
+    const int nb = p.k >> 5;
+    const size_t smem = (size_t)xq_stride(nb) * p.batch;
+    if (smem > (size_t)lc.max_smem_optin) return QG_ERR_UNSUPPORTED;
+    if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
+    int rows_ctas = (p.n + 7) / 8;
+    int grid = lc.sm_count * 8;
+    if (EPI == EPI_ARGMAX) grid = lc.sm_count * 4 < VOCAB_MAX_CTAS ? lc.sm_count * 4 : VOCAB_MAX_CTAS;
+    if (grid > rows_ctas) grid = rows_ctas;
+    if (grid < 1) grid = 1;
+    return launch_kernel(kern, dim3(grid), dim3(256), smem, lc, p);
+}
+
+int launch_plain(const PlainParams& p, int bits, int epi, const LaunchCtx& lc) {
+    const int bc = p.batch <= 1 ? 1 : p.batch <= 2 ? 2 : p.batch <= 4 ? 4 : p.batch <= 8 ? 8 : 16;
+    if (epi == EPI_ARGMAX) return bits == 4 ? launch_plain_t<4, 1, EPI_ARGMAX>(p, lc) : launch_plain_t<6, 1, EPI_ARGMAX>(p, lc);
+#define QG_CASE(B)                                                                                  \
+    case B:                                                                                         \
+        return bits == 4 ? launch_plain_t<4, B, EPI_STORE>(p, lc) : launch_plain_t<6, B, EPI_STORE>(p, lc);
+    switch (bc) {
+        QG_CASE(1)
+        QG_CASE(2)
+        QG_CASE(4)
+        QG_CASE(8)
+        QG_CASE(16)
+    }
+#undef QG_CASE
+    return QG_ERR_UNSUPPORTED;
+}
+
+int launch_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, const LaunchCtx& lc) {
+    const long long blocks = (long long)batch * (k >> 5);
+    long long grid = (blocks + 7) / 8;
+    if (grid > lc.sm_count * 16) grid = lc.sm_count * 16;
+    return launch_kernel(quantize_act_kernel, dim3((unsigned)grid), dim3(256), 0, lc, x, k, batch, xq, xs, xsum);
+}
+
+int launch_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,
+                     const LaunchCtx& lc) {
+    const long long total = (long long)n * (k >> 5);
+    long long grid = (total + 255) / 256;
+    if (grid > lc.sm_count * 16) grid = lc.sm_count * 16;
+    if (bits == 4)
+        return launch_kernel(blockdots_kernel<4>, dim3((unsigned)grid), dim3(256), 0, lc, lo, hi, n, k, xq, dots);
+    return launch_kernel(blockdots_kernel<6>, dim3((unsigned)grid), dim3(256), 0, lc, lo, hi, n, k, xq, dots);
+}
+
+}  // namespace qg

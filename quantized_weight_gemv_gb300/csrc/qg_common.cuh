@@ -1,0 +1,297 @@
+// Shared device helpers of the quantized-weight GEMV kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qgemv.h"
+
+namespace qg {
+
+// Codes OR-ed into the device error word (its address is a kernel parameter) by a
+// kernel whose bounded wait ran out.  Host side: qg_device_error() reads and clears it.
+enum : unsigned { ERR_WAIT_FULL = 1u, ERR_WAIT_EMPTY = 2u, ERR_WAIT_DRAIN = 4u };
+
+constexpr int WARP = 32;
+// 1 s: far beyond any legitimate wait of these kernels, short enough to keep the context alive.
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ unsigned short ldg_stream2(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float half_bits_to_float(unsigned short b) {
+    return __half2float(__ushort_as_half(b));
+}
+
+// ---------------------------------------------------------------- activation quantisation
+// One block of 32 values held one per lane: s = max|x| / 127 (IEEE fp32 division),
+// q = clamp(round-half-even(x / s), -127, 127), q = 0 when s == 0.  Returns q; s and
+// the block sum S are returned through references (valid in every lane).
+__device__ __forceinline__ int quantize_lane(float x, float& s, int& S) {
+    float a = fabsf(x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    s = __fdiv_rn(a, 127.0f);
+    int q = 0;
+    if (s != 0.0f) {
+        q = __float2int_rn(__fdiv_rn(x, s));
+        q = max(-127, min(127, q));
+    }
+    int t = q;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    S = t;
+    return q;
+}
+
+// Shared-memory image of a quantised activation column with nb blocks:
+//   lo[nb][16] int8 : elements 0..15 of each block;  hi[nb][16] int8 : elements 16..31;
+//   s[nb] fp32 ; S[nb] fp32 (block sums, exact in fp32).
+// The split halves let a lane fetch the 16 activations that meet the low (or high)
+// nibbles of its 16-byte code block with one conflict-free 128-bit load.
+struct XqView {
+    int8_t* lo;
+    int8_t* hi;
+    float* s;
+    float* S;
+};
+__device__ __forceinline__ XqView xq_view(unsigned char* base, int nb) {
+    XqView v;
+    v.lo = reinterpret_cast<int8_t*>(base);
+    v.hi = reinterpret_cast<int8_t*>(base + 16 * nb);
+    v.s = reinterpret_cast<float*>(base + 32 * nb);
+    v.S = reinterpret_cast<float*>(base + 36 * nb);
+    return v;
+}
+__host__ __device__ constexpr int xq_bytes(int nb) { return 40 * nb; }
+
+// Cooperative quantisation of x[k] into an XqView by NT threads (t = 0..NT-1, whole
+// warps).  Thread t takes float4 number i*NT + t: eight consecutive lanes hold one
+// block of 32, so a block's max and sum need three shuffles.  All loads of a round
+// are issued before any use, so the prologue costs about one L2 round trip per
+// CHUNK float4 per thread instead of one per block.
+template <int NT>
+__device__ __forceinline__ void quantize_x_coop(const float* __restrict__ x, int k, XqView v, int t) {
+    constexpr int CHUNK = 8;
+    const int nf4 = k >> 2;  // a multiple of 8
+    const int m = t & 7;     // float4 index within the block
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (int base = 0; base < nf4; base += NT * CHUNK) {
+        float4 r[CHUNK];
+#pragma unroll
+        for (int i = 0; i < CHUNK; ++i) {
+            const int idx = base + i * NT + t;
+            r[i] = idx < nf4 ? __ldg(x4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < CHUNK; ++i) {
+            const int idx = base + i * NT + t;
+            float a = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            const float s = __fdiv_rn(a, 127.0f);
+            int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+            if (s != 0.0f) {
+                q0 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].x, s))));
+                q1 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].y, s))));
+                q2 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].z, s))));
+                q3 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].w, s))));
+            }
+            int S = q0 + q1 + q2 + q3;
+            S += __shfl_xor_sync(0xffffffffu, S, 1);
+            S += __shfl_xor_sync(0xffffffffu, S, 2);
+            S += __shfl_xor_sync(0xffffffffu, S, 4);
+            if (idx < nf4) {
+                const int b = idx >> 3;
+                const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
+                                        ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+                int8_t* dst = m < 4 ? v.lo + 16 * b + 4 * m : v.hi + 16 * b + 4 * (m - 4);
+                *reinterpret_cast<uint32_t*>(dst) = packed;
+                if (m == 0) {
+                    v.s[b] = s;
+                    v.S[b] = (float)S;
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- unpack + dp4a block dot
+// 16 code bytes of a Q4 block: word w (bytes 4w..4w+3) carries codes 4w..4w+3 in its
+// low nibbles and codes 16+4w..16+4w+3 in its high nibbles.
+struct Codes32 {
+    uint32_t lo[4];  // codes 0..15, one per byte
+    uint32_t hi[4];  // codes 16..31
+};
+
+__device__ __forceinline__ Codes32 unpack_q4(uint4 c) {
+    Codes32 r;
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r.lo[i] = w[i] & 0x0F0F0F0Fu;
+        r.hi[i] = (w[i] >> 4) & 0x0F0F0F0Fu;
+    }
+    return r;
+}
+
+// Q6: the 8 hi bytes hold the top two bits of codes t, t+8, t+16, t+24 in byte t.
+// Codes 4w..4w+3 sit in bytes 4(w&1).. of word h[w&1] at bit pair w>>1; codes
+// 16+4w.. at bit pair 2 + (w>>1).
+__device__ __forceinline__ Codes32 unpack_q6(uint4 c, uint2 h) {
+    Codes32 r = unpack_q4(c);
+    const uint32_t hw[2] = {h.x, h.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t src = hw[i & 1];
+        r.lo[i] |= ((src >> (2 * (i >> 1))) & 0x03030303u) << 4;
+        r.hi[i] |= ((src >> (4 + 2 * (i >> 1))) & 0x03030303u) << 4;
+    }
+    return r;
+}
+
+// sum over the 32 codes of code * xq (codes 0..63 are non-negative in a signed byte)
+__device__ __forceinline__ int block_dot(const Codes32& c, uint4 xlo, uint4 xhi) {
+    int d = __dp4a((int)c.lo[0], (int)xlo.x, 0);
+    d = __dp4a((int)c.lo[1], (int)xlo.y, d);
+    d = __dp4a((int)c.lo[2], (int)xlo.z, d);
+    d = __dp4a((int)c.lo[3], (int)xlo.w, d);
+    d = __dp4a((int)c.hi[0], (int)xhi.x, d);
+    d = __dp4a((int)c.hi[1], (int)xhi.y, d);
+    d = __dp4a((int)c.hi[2], (int)xhi.z, d);
+    d = __dp4a((int)c.hi[3], (int)xhi.w, d);
+    return d;
+}
+
+// s_b * (scale * D + min * S_b) in fp32
+__device__ __forceinline__ float block_combine(int D, float d, float m, float s, float S) {
+    return s * fmaf(d, (float)D, m * S);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------- soft-cap + argmax ordering
+__device__ __forceinline__ float softcap_apply(float z, float c) {
+    return c > 0.0f ? c * tanhf(__fdiv_rn(z, c)) : z;
+}
+
+// (value, index) order for the argmax: larger value first, then lower index; NaN never wins.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    if (v != v) return false;
+    if (bv != bv) return true;
+    return v > bv || (v == bv && i < bi);
+}
+
+struct ArgmaxPartial {
+    float value;
+    int index;
+};
+
+// Workspace of the vocabulary argmax: a counter, then one partial per CTA.
+constexpr int VOCAB_MAX_CTAS = 4096;
+struct VocabWorkspace {
+    unsigned int counter;
+    unsigned int pad[63];
+    ArgmaxPartial part[VOCAB_MAX_CTAS];
+};
+
+// Block-wide (value, index) reduction, then the last CTA to finish reduces every
+// CTA's partial, writes the index and re-arms the counter.  No CTA waits on another.
+// Called by all threads of the block.
+__device__ __forceinline__ void argmax_finish(float bv, int bi, VocabWorkspace* ws, int32_t* out,
+                                              ArgmaxPartial* sred /* >= blockDim/32 entries */,
+                                              int* sflag) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) {
+            bv = ov;
+            bi = oi;
+        }
+    }
+    if (lane == 0) sred[wid] = ArgmaxPartial{bv, bi};
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < nw; ++w)
+            if (better(sred[w].value, sred[w].index, bv, bi)) {
+                bv = sred[w].value;
+                bi = sred[w].index;
+            }
+        ws->part[blockIdx.x] = ArgmaxPartial{bv, bi};
+        __threadfence();
+        unsigned prev = atomicAdd(&ws->counter, 1u);
+        *sflag = (prev == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (*sflag) {
+        __threadfence();
+        float v = __int_as_float(0x7fc00000);  // NaN: loses to any number
+        int i = 0x7fffffff;
+        for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+            float cv = __ldcg(&ws->part[c].value);
+            int ci = __ldcg(&ws->part[c].index);
+            if (better(cv, ci, v, i)) {
+                v = cv;
+                i = ci;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, v, o);
+            int oi = __shfl_xor_sync(0xffffffffu, i, o);
+            if (better(ov, oi, v, i)) {
+                v = ov;
+                i = oi;
+            }
+        }
+        __syncthreads();  // sred reuse
+        if (lane == 0) sred[wid] = ArgmaxPartial{v, i};
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < nw; ++w)
+                if (better(sred[w].value, sred[w].index, v, i)) {
+                    v = sred[w].value;
+                    i = sred[w].index;
+                }
+            // every value NaN (or no rows): index 0, as the lowest index
+            *out = (i == 0x7fffffff) ? 0 : i;
+            ws->counter = 0u;
+        }
+    }
+}
+
+}  // namespace qg

@@ -1,0 +1,98 @@
+// Internal declarations shared by the kernel files and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qg_common.cuh"
+
+namespace qg {
+
+enum : int { EPI_STORE = 0, EPI_ARGMAX = 1 };
+
+// per-column shared-memory stride of a quantised activation (16-byte aligned)
+__host__ __device__ constexpr int xq_stride(int nb) { return (xq_bytes(nb) + 15) & ~15; }
+
+struct PlainParams {
+    const uint8_t* lo;
+    const uint8_t* hi;
+    const uint16_t* scale;
+    const uint16_t* min;
+    int n, k, batch;
+    const float* x;  // [batch][k]
+    float* y;        // EPI_STORE: [batch][n]; EPI_ARGMAX: logits [n] or null
+    float softcap;
+    int32_t* argmax;
+    VocabWorkspace* ws;
+};
+
+struct StreamParams {
+    const uint8_t* lo;
+    const uint8_t* hi;
+    const uint16_t* scale;
+    const uint16_t* min;
+    int n, k, batch;
+    int log2nb;  // log2(k/32)
+    int stages;  // ring depth
+    const float* x;
+    float* y;
+    float softcap;
+    int32_t* argmax;
+    VocabWorkspace* ws;
+    unsigned int* err;  // device error word
+};
+
+struct CqParams {
+    const uint8_t* idx;
+    const uint16_t* codebook;
+    const uint16_t* row_scale;
+    int n, k, group, row_start, row_count;
+    float inv_sqrt_group;
+    const float* x;
+    float* y;
+};
+
+// Per-call launch context resolved by the C-ABI layer.
+struct LaunchCtx {
+    cudaStream_t stream;
+    unsigned flags;
+    int device;
+    int sm_count;
+    int max_smem_optin;
+    unsigned int* err;  // device address of the error word
+};
+
+int ensure_smem_attr(const void* kernel, size_t smem, const LaunchCtx& lc);
+
+template <typename... KArgs, typename... Args>
+int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, const LaunchCtx& lc, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = lc.stream;
+    cudaLaunchAttribute attr[1];
+    if (lc.flags & QG_FLAG_PDL) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QG_ERR_CUDA;
+    }
+    return QG_OK;
+}
+
+int launch_plain(const PlainParams& p, int bits, int epi, const LaunchCtx& lc);
+// returns QG_ERR_UNSUPPORTED when the shape has no bulk-copy variant
+int launch_stream(const StreamParams& p, int bits, int epi, const LaunchCtx& lc);
+bool stream_supported(int bits, int n, int k, int batch, int epi);
+int launch_cq(const CqParams& p, const LaunchCtx& lc);
+int launch_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, const LaunchCtx& lc);
+int launch_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,
+                     const LaunchCtx& lc);
+
+}  // namespace qg

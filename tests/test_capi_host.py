@@ -1,0 +1,122 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+declared entry point, and rejects bad arguments with the documented status
+before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_weight_gemv_gb300 as qg
+from quantized_weight_gemv_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qg.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "qgemv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_functions()
+    for n in ("qgemv_q4", "qgemv_q6", "qgemv_batched", "cq_fwht_matvec", "vocab_softcap_argmax"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in qg.SIGNATURES, n  # and the binding knows its signature
+
+
+def test_status_strings_and_version(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert qg.status_string(code) not in ("", "unknown status")
+    assert qg.status_string(-99) == "unknown status"
+    assert lib.qg_version() >= 100
+    assert lib.qg_vocab_workspace_bytes() >= 256 + 8 * 152
+
+
+P = ctypes.c_void_p
+A16 = P(0x10000)      # a 16-byte aligned stand-in address: never dereferenced on these paths
+MIS = P(0x10004)      # misaligned
+
+
+def test_q4_validation(lib):
+    f = lib.qgemv_q4
+    assert f(A16, A16, A16, 4, 48, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG      # k % 32
+    assert f(A16, A16, A16, -1, 64, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG     # n < 0
+    assert f(A16, A16, A16, 4, 0, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG       # k == 0
+    assert f(A16, A16, A16, 4, 65536 + 32, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(None, A16, A16, 4, 64, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(A16, A16, A16, 4, 64, None, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(A16, A16, A16, 4, 64, A16, None, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(MIS, A16, A16, 4, 64, A16, A16, 0, None) == qg.QG_ERR_ALIGNMENT
+    assert f(A16, A16, MIS, 4, 64, A16, A16, 0, None) == qg.QG_ERR_ALIGNMENT
+    assert f(A16, A16, A16, 4, 64, MIS, A16, 0, None) == qg.QG_ERR_ALIGNMENT
+    assert f(A16, A16, A16, 4, 64, A16, MIS, 0, None) == qg.QG_ERR_ALIGNMENT
+    assert f(A16, A16, A16, 0, 64, A16, A16, 0, None) == qg.QG_OK                   # n == 0: nothing to do
+    assert f(None, None, None, 0, 64, None, None, 0, None) == qg.QG_OK
+
+
+def test_q6_and_batched_validation(lib):
+    assert lib.qgemv_q6(A16, None, A16, A16, 4, 64, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert lib.qgemv_q6(A16, MIS, A16, A16, 4, 64, A16, A16, 0, None) == qg.QG_ERR_ALIGNMENT
+    b = lib.qgemv_batched
+    assert b(5, A16, None, A16, A16, 4, 64, 1, A16, A16, 0, None) == qg.QG_ERR_UNSUPPORTED
+    assert b(4, A16, A16, A16, A16, 4, 64, 1, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG  # hi given for Q4
+    assert b(4, A16, None, A16, A16, 4, 64, 0, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert b(4, A16, None, A16, A16, 4, 64, 17, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert b(4, A16, None, A16, A16, 4, 16384, 16, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG  # batch*k too big
+
+
+def test_cq_validation(lib):
+    f = lib.cq_fwht_matvec
+    assert f(A16, A16, A16, 8, 512, 100, 0, 8, A16, A16, 0, None) == qg.QG_ERR_UNSUPPORTED
+    assert f(A16, A16, A16, 8, 768, 512, 0, 8, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG   # k % group
+    assert f(A16, A16, A16, 8, 512, 512, 4, 5, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG   # range past n
+    assert f(A16, A16, A16, 8, 512, 512, -1, 2, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(A16, A16, A16, 8, 512, 512, 0, 8, MIS, A16, 0, None) == qg.QG_ERR_ALIGNMENT
+    assert f(A16, A16, A16, 8, 32768, 512, 0, 8, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(A16, A16, A16, 8, 512, 512, 3, 0, A16, A16, 0, None) == qg.QG_OK   # empty range
+
+
+def test_vocab_validation(lib):
+    f = lib.vocab_softcap_argmax
+    ws = lib.qg_vocab_workspace_bytes()
+    assert f(6, A16, A16, A16, A16, 0, 64, A16, 30.0, None, A16, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(6, A16, A16, A16, A16, 8, 64, A16, 30.0, None, A16, None, ws, 0, None) == qg.QG_ERR_WORKSPACE
+    assert f(6, A16, A16, A16, A16, 8, 64, A16, 30.0, None, A16, A16, ws - 1, 0, None) == qg.QG_ERR_WORKSPACE
+    assert f(6, A16, A16, A16, A16, 8, 64, A16, 30.0, None, None, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(6, A16, A16, A16, A16, 8, 64, A16, float("nan"), None, A16, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(6, A16, A16, A16, A16, 8, 64, A16, 30.0, MIS, A16, A16, ws, 0, None) == qg.QG_ERR_ALIGNMENT
+    assert f(3, A16, A16, A16, A16, 8, 64, A16, 30.0, None, A16, A16, ws, 0, None) == qg.QG_ERR_UNSUPPORTED
+
+
+def test_exposed_steps_validation(lib):
+    assert lib.qg_quantize_act(A16, 48, 1, A16, A16, A16, None) == qg.QG_ERR_INVALID_ARG
+    assert lib.qg_quantize_act(A16, 64, 0, A16, A16, A16, None) == qg.QG_ERR_INVALID_ARG
+    assert lib.qg_quantize_act(MIS, 64, 1, A16, A16, A16, None) == qg.QG_ERR_ALIGNMENT
+    assert lib.qg_blockdots(5, A16, None, 4, 64, A16, A16, None) == qg.QG_ERR_UNSUPPORTED
+    assert lib.qg_blockdots(4, A16, None, 4, 64, MIS, A16, None) == qg.QG_ERR_ALIGNMENT
+    assert lib.qg_blockdots(4, A16, None, 0, 64, None, None, None) == qg.QG_OK
+    assert lib.qg_device_error(None) == qg.QG_ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    t = torch.zeros(4, 32, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        qg.qgemv_q4(t, torch.zeros(4, 1, dtype=torch.float16), torch.zeros(4, 1, dtype=torch.float16),
+                    torch.zeros(64))

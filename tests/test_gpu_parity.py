@@ -1,0 +1,283 @@
+"""GPU parity: the CUDA kernels, called through the C ABI, against the CPU oracle.
+
+Integer work (activation codes, block dots, argmax) must match bit for bit;
+fp32 outputs must be within TOL = 1e-3 of the fp64 oracle by the normwise rule
+|y - ref| <= TOL * max(|ref|, rms(ref)).
+"""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+import quantized_weight_gemv_gb300 as qg
+from tests._gpu import DEV, TOL, assert_close, dev_w, gpu_gemv, oracle_gemv_par
+from tests._layout import make_w
+
+pytestmark = pytest.mark.gpu
+
+FLAGS = [0, qg.QG_FLAG_PLAIN, qg.QG_FLAG_PDL]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from quantized_weight_gemv_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    yield
+    assert qg.device_error() == 0
+
+
+# ---------------------------------------------------------------- activation quantisation (bit-exact)
+def _special_x(k, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(k).astype(np.float32)
+    nb = k // 32
+    if nb > 1:
+        x[32:64] = 0.0                           # all-zero block
+    if nb > 2:
+        x[64:96] = 0.0
+        x[64 + 7] = -3.5                         # unit vector
+    if nb > 3:
+        x[96:128] *= 1e-30                       # tiny (subnormal scale)
+    if nb > 4:
+        x[128:160] = np.float32(127.0) * np.round(rng.standard_normal(32) * 20) / 127  # exact halves
+    if nb > 5:
+        x[160:192] *= 1e30
+    return x
+
+
+@pytest.mark.parametrize("k,batch", [(32, 1), (2048, 1), (16384, 1), (1024, 5)])
+def test_quantize_act_bit_exact(k, batch):
+    X = np.stack([_special_x(k, 100 + b) for b in range(batch)])
+    xq, xs, xsum = qg.qg_quantize_act(torch.from_numpy(X).to(DEV))
+    for b in range(batch):
+        oq, os_, oS = oracle.quantize_act(X[b])
+        assert np.array_equal(xq[b].cpu().numpy(), oq)
+        assert np.array_equal(xs[b].cpu().numpy().view(np.uint32), os_.view(np.uint32))
+        assert np.array_equal(xsum[b].cpu().numpy(), oS)
+
+
+# ---------------------------------------------------------------- block dots (bit-exact)
+@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("n,k", [(1, 32), (37, 96), (300, 2048)])
+def test_blockdots_bit_exact(bits, n, k):
+    rng = np.random.default_rng(n + k + bits)
+    q = rng.integers(0, 16 if bits == 4 else 64, size=(n, k), dtype=np.uint8)
+    w = make_w(bits, q, 1.0, 0.0)
+    xq = rng.integers(-127, 128, size=k).astype(np.int8)
+    wd = dev_w(w)
+    D = qg.qg_blockdots(bits, wd["lo"], wd.get("hi"), torch.from_numpy(xq).to(DEV)).cpu().numpy()
+    assert np.array_equal(D, oracle.blockdots(w, xq))
+
+
+def test_blockdots_extremes_bit_exact():
+    """Largest magnitudes: codes 63 against xq = +-127 (|D| = 32*63*127)."""
+    k = 64
+    q = np.full((2, k), 63, np.uint8)
+    q[1, ::2] = 0
+    w = make_w(6, q, 1.0, 0.0)
+    wd = dev_w(w)
+    for v in (127, -127):
+        xq = np.full(k, v, np.int8)
+        D = qg.qg_blockdots(6, wd["lo"], wd["hi"], torch.from_numpy(xq).to(DEV)).cpu().numpy()
+        assert np.array_equal(D, oracle.blockdots(w, xq))
+        assert D[0, 0] == 32 * 63 * v
+
+
+# ---------------------------------------------------------------- GEMV
+SHAPES = [(1, 32), (7, 96), (33, 256), (100, 512), (1000, 1024), (1024, 1024), (333, 2048), (2049, 2048),
+          (77, 4096), (19, 8192), (40, 16384), (3, 1056), (5, 32768)]
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("n,k", SHAPES)
+@pytest.mark.parametrize("flags", FLAGS)
+def test_gemv_random(bits, n, k, flags):
+    w = datagen.make_quantized(bits, 7 * n + k, n, k)
+    x = datagen.normal_f32(7 * n + k, 1, k)
+    y = gpu_gemv(dev_w(w), x, flags)
+    assert_close(y, oracle.gemv(w, x))
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_gemv_special_activations(bits):
+    n, k = 64, 2048
+    w = datagen.make_quantized(bits, 55, n, k)
+    wd = dev_w(w)
+    for x in (np.zeros(k, np.float32), _special_x(k, 3)):
+        for flags in (0, qg.QG_FLAG_PLAIN):
+            y = gpu_gemv(wd, x, flags)
+            ref = oracle.gemv(w, x)
+            if not x.any():
+                assert np.array_equal(y, np.zeros(n))
+            else:
+                assert_close(y, ref)
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_gemv_constant_code_closed_form(bits):
+    """Constant-code rows: y = sum_b s_b * (scale*c + min) * S_b, checked against the oracle's closed form."""
+    k = 1024
+    cvals = [0, 5, 15] if bits == 4 else [0, 33, 63]
+    q = np.array([[c] * k for c in cvals], np.uint8)
+    w = make_w(bits, q, 0.0078125, -0.0625)
+    x = datagen.normal_f32(12, 1, k)
+    y = gpu_gemv(dev_w(w), x)
+    xq, s, S = oracle.quantize_act(x)
+    ref = np.array([sum(float(s[b]) * (0.0078125 * c - 0.0625) * int(S[b]) for b in range(k // 32)) for c in cvals])
+    assert_close(y, ref)
+
+
+def test_gemv_paths_agree():
+    """The bulk-copy ring and the plain-load kernel give the same rows to fp32 rounding."""
+    n, k = 4096, 2048
+    w = datagen.make_quantized(4, 99, n, k)
+    x = datagen.normal_f32(99, 1, k)
+    wd = dev_w(w)
+    a = gpu_gemv(wd, x, 0)
+    b = gpu_gemv(wd, x, qg.QG_FLAG_PLAIN)
+    assert oracle.normwise_error(a, b) < 1e-5
+
+
+def test_gemv_outputs_only_their_rows():
+    """Guard bands around y stay untouched (no out-of-range stores)."""
+    n, k = 333, 2048
+    w = datagen.make_quantized(4, 5, n, k)
+    x = torch.from_numpy(datagen.normal_f32(5, 1, k)).to(DEV)
+    wd = dev_w(w)
+    for flags in (0, qg.QG_FLAG_PLAIN):
+        buf = torch.full((n + 64,), float("nan"), device=DEV)
+        y = buf[16:16 + n]
+        qg.qgemv_q4(wd["lo"], wd["scale"], wd["min"], x, y=y, flags=flags)
+        host = buf.cpu().numpy()
+        assert np.all(np.isnan(host[:16])) and np.all(np.isnan(host[16 + n:]))
+        assert np.all(np.isfinite(host[16:16 + n]))
+
+
+def test_gemv_empty_is_noop():
+    z = torch.zeros(0, 16, dtype=torch.uint8, device=DEV)
+    h = torch.zeros(0, 1, dtype=torch.float16, device=DEV)
+    y = qg.qgemv_q4(z, h, h, torch.zeros(32, device=DEV))
+    assert y.numel() == 0
+
+
+# ---------------------------------------------------------------- batched
+@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
+def test_batched(bits, batch, flags):
+    n, k = 1000, 2048
+    w = datagen.make_quantized(bits, 300 + batch, n, k)
+    X = datagen.normal_f32(300 + batch, 1, batch * k).reshape(batch, k)
+    wd = dev_w(w)
+    Y = qg.qgemv_batched(bits, wd["lo"], wd.get("hi"), wd["scale"], wd["min"], torch.from_numpy(X).to(DEV),
+                         flags=flags).cpu().numpy()
+    for b in range(batch):
+        assert_close(Y[b], oracle.gemv(w, X[b]))
+
+
+def test_batched_columns_match_single():
+    n, k, batch = 512, 2048, 4
+    w = datagen.make_quantized(4, 31, n, k)
+    X = datagen.normal_f32(31, 1, batch * k).reshape(batch, k)
+    wd = dev_w(w)
+    Y = qg.qgemv_batched(4, wd["lo"], None, wd["scale"], wd["min"], torch.from_numpy(X).to(DEV)).cpu().numpy()
+    for b in range(batch):
+        assert oracle.normwise_error(Y[b], gpu_gemv(wd, X[b])) < 1e-5
+
+
+# ---------------------------------------------------------------- vocab soft-cap + argmax
+def _vocab_check(w, x, softcap, flags=0, ws=None):
+    wd = dev_w(w)
+    xt = torch.from_numpy(x).to(DEV)
+    logits, am = qg.vocab_softcap_argmax(w["bits"], wd["lo"], wd.get("hi"), wd["scale"], wd["min"], xt, softcap,
+                                         ws=ws, flags=flags)
+    l = logits.cpu().numpy()
+    idx = int(am.item())
+    ref_l = oracle.softcap(oracle_gemv_par(w, x), softcap)
+    assert_close(l, ref_l)
+    # exact self-consistency: the index is the lowest argmax of the returned logits
+    assert idx == oracle.argmax(l)
+    # against the oracle wherever its top-2 margin exceeds the tolerance
+    order = np.argsort(-ref_l, kind="stable")
+    rms = float(np.sqrt(np.mean(ref_l ** 2)))
+    margin = ref_l[order[0]] - ref_l[order[1]] if ref_l.size > 1 else np.inf
+    if margin > 2 * TOL * max(abs(ref_l[order[0]]), rms):
+        assert idx == oracle.argmax(ref_l)
+    # without logits the index is the same
+    _, am2 = qg.vocab_softcap_argmax(w["bits"], wd["lo"], wd.get("hi"), wd["scale"], wd["min"], xt, softcap,
+                                     logits=None, ws=ws, flags=flags)
+    assert int(am2.item()) == idx
+    return idx
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("n,k", [(1, 32), (1000, 256), (5000, 2048), (3001, 1056), (700, 16384)])
+@pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
+def test_vocab_random(bits, n, k, flags):
+    w = datagen.make_quantized(bits, n + 3 * k, n, k)
+    x = datagen.normal_f32(n + 3 * k, 1, k)
+    _vocab_check(w, x, 30.0, flags)
+
+
+@pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
+def test_vocab_planted_maximum_and_ties(flags):
+    n, k = 20000, 2048
+    rng = np.random.default_rng(8)
+    q = rng.integers(0, 64, size=(n, k), dtype=np.uint8)
+    q[12345] = 63
+    q[17000] = 63      # an exact tie with a higher index: the lower one wins
+    w = make_w(6, q, 0.001, 0.0)
+    x = (np.abs(rng.standard_normal(k)) + 0.1).astype(np.float32)
+    assert _vocab_check(w, x, 30.0, flags) == 12345
+
+
+def test_vocab_softcap_off_and_workspace_reuse():
+    n, k = 4096, 2048
+    w = datagen.make_quantized(6, 21, n, k)
+    x = datagen.normal_f32(21, 1, k)
+    ws = qg.vocab_workspace(DEV)
+    a = _vocab_check(w, x, 0.0, ws=ws)
+    b = _vocab_check(w, x, 30.0, ws=ws)
+    assert a == b  # the cap is monotone
+    assert int(ws[:4].view(torch.int32).item()) == 0  # the completion counter is re-armed
+
+
+# ---------------------------------------------------------------- CQ
+@pytest.mark.parametrize("group", [128, 256, 512, 1024])
+@pytest.mark.parametrize("n,k_groups", [(1, 1), (1024, 1), (8192, 1), (333, 2), (50, 5)])
+def test_cq(group, n, k_groups):
+    k = group * k_groups
+    m = datagen.make_cq(4 + group, n, k)
+    x = datagen.normal_f32(4 + group, 1, k)
+    md = dev_w(m)
+    y = qg.cq_fwht_matvec(md["idx"], md["codebook"], md["row_scale"], torch.from_numpy(x).to(DEV), group)
+    assert_close(y.cpu().numpy(), oracle.cq_matvec(m, x, group))
+
+
+def test_cq_row_ranges():
+    n, k = 8192, 512
+    m = datagen.make_cq(4, n, k)
+    x = datagen.normal_f32(4, 1, k)
+    md = dev_w(m)
+    xt = torch.from_numpy(x).to(DEV)
+    full = oracle.cq_matvec(m, x, 512)
+    for start, count in ((0, 1), (5, 100), (8000, 192), (4096, 0), (1, 8191)):
+        y = qg.cq_fwht_matvec(md["idx"], md["codebook"], md["row_scale"], xt, 512, start, count).cpu().numpy()
+        if count:
+            assert_close(y, full[start:start + count])
+
+
+def test_cq_constant_index_closed_form():
+    k, g = 512, 512
+    idx = np.full((4, k), 7, np.uint8)
+    from tests._layout import f16_bits, pack_cq
+    cb = np.linspace(-0.1, 0.1, 16).astype(np.float32)
+    m = {"n": 4, "k": k, "idx": pack_cq(idx), "codebook": f16_bits(cb),
+         "row_scale": f16_bits(np.array([0.5, 1.0, 1.25, 1.5], np.float32))}
+    x = datagen.normal_f32(44, 1, k)
+    md = dev_w(m)
+    y = qg.cq_fwht_matvec(md["idx"], md["codebook"], md["row_scale"], torch.from_numpy(x).to(DEV), g).cpu().numpy()
+    ref = (m["row_scale"].view(np.float16).astype(np.float64) * float(np.float16(cb[7])) * np.sqrt(g) * float(x[0]))
+    assert_close(y, ref)

@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
     if (threadIdx.x == 0) pdl_launch_dependents();
 
     for (int c = 0; c < p.batch; ++c)
-        quantize_to_smem(p.x + (size_t)c * p.k, nb, xq_view(smem + c * xstride, nb), wid, 8);
+        quantize_x_coop<256>(p.x + (size_t)c * p.k, p.k, xq_view(smem + c * xstride, nb), threadIdx.x);
     __syncthreads();
 
     float bv = __int_as_float(0x7fc00000);

@@ -1,0 +1,363 @@
+// Streaming quantized-weight GEMV: persistent CTAs whose warps each pull their own
+// weight stages through a private shared-memory ring with the bulk-copy engine (TMA).
+//
+// Decode is bandwidth-bound: every weight byte is read once per token (oxinfer
+// README, "Performance"; genie-ai-runtime, "The decode arc").  The kernel is shaped
+// for that:
+//  * CTA b owns the contiguous rows [b*n/G, (b+1)*n/G) of the matrix (G = grid).
+//  * A stage is 256 consecutive blocks of 32 weights in row-major order: R = 256/nb
+//    whole rows when nb = k/32 <= 256, else one 256-block part of a row.  Each
+//    stage is one contiguous span per plane (codes, [hi,] scale, min), fetched by
+//    one cp.async.bulk per plane, completion tracked by an mbarrier.
+//  * Warp w of the CTA owns units w, w+W, w+2W, ... (a unit is a stage's rows, or
+//    one whole row of nb/256 stages when nb > 256) and keeps D stages of its own in
+//    flight in D private slots.  Its lane 0 issues the copies.  The first D are
+//    issued before griddepcontrol.wait, so under programmatic dependent launch the
+//    weight stream overlaps the tail of the preceding kernel.
+//  * A warp moves a landed stage from shared memory into registers, refills the
+//    slot with its next stage at once, and only then computes: lane l takes blocks
+//    l + 32j (j < 8) of the stage, dots each with the int8 activation by dp4a over
+//    nibbles unpacked from 32-bit words (genie-ai-runtime, "The decode arc": dp4a
+//    int8 MMVQ "instead of dequant-to-fp"; its uint32 fast path for the dequant
+//    loop), applies the fp32 block combine s_b * (scale * D + min * S_b), and
+//    reduces the stage's rows together with a halving shuffle tree (warp-per-row
+//    reduction: genie-ai-runtime, "The decode arc"; one 32-lane group per row in
+//    needle.js "Inference backends", "TypeGPU").  No barrier couples the warps.
+//  * A lane's block positions are the same in every stage, so for short rows its
+//    activation words live in registers; for long rows they are read from shared
+//    memory, stored as split halves so that the 128-bit reads are conflict-free.
+//  * Every wait is bounded (mbarrier try_wait against %globaltimer); on expiry the
+//    kernel ORs a code into the library's device error word and stops.
+#pragma once
+
+#include "qg_internal.h"
+
+namespace qg {
+namespace stream {
+
+constexpr int SBW = 256;  // blocks per stage
+constexpr int JPL = 8;    // blocks per lane per stage
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of the given parity to complete; false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+// Slot layout: codes[256][16] | [hi[256][8]] | scale[256] | min[256]
+template <int BITS>
+struct Slot {
+    static constexpr int BPB = 16 + (BITS == 6 ? 8 : 0) + 4;
+    static constexpr int BYTES = SBW * BPB;
+    static constexpr int HI = SBW * 16;
+    static constexpr int SC = SBW * (BITS == 6 ? 24 : 16);
+    static constexpr int MN = SC + SBW * 2;
+};
+
+// Halving reduction over the lane bits [0, LOG2SEG): V values per lane, each to be
+// summed over the 2^LOG2SEG lanes of a segment.  Step s pairs lanes across bit
+// LOG2SEG-1-s; the lower lane keeps (and sums) the lower half of the values still
+// held, the upper lane the upper half, so V values cost V-1 shuffles instead of
+// V*LOG2SEG.  The bits left after log2(V) steps are summed with plain xor steps.
+// On return v[0] of lane l is the segment total of value index
+// (l & (2^LOG2SEG - 1)) >> (LOG2SEG - log2(V)).
+template <int V, int LOG2SEG>
+__device__ __forceinline__ void halving_reduce(float (&v)[V]) {
+    static_assert((V & (V - 1)) == 0 && V >= 1, "V power of two");
+    const int lane = threadIdx.x & 31;
+    int cur = V;
+    int off = 1 << (LOG2SEG - 1);
+#pragma unroll
+    for (int step = 0; (1 << step) < V; ++step) {
+        const int half = cur >> 1;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < V / 2; ++i) {
+            if (i < half) {
+                const float send = upper ? v[i] : v[i + half];
+                const float keep = upper ? v[i + half] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+        cur = half;
+        off >>= 1;
+    }
+#pragma unroll
+    for (; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+}
+
+// byte offset of the activation columns after `nslots` slots and their mbarriers
+__host__ __device__ constexpr size_t xq_offset(int nslots, int slot_bytes) {
+    return (((size_t)nslots * (size_t)(slot_bytes + 8)) + 15) & ~(size_t)15;
+}
+
+template <int EPI, int BC>
+__device__ __forceinline__ void emit_row(const StreamParams& p, long long row, const float (&v)[BC], float& bv,
+                                         int& bi) {
+    if constexpr (EPI == EPI_STORE) {
+#pragma unroll
+        for (int c = 0; c < BC; ++c)
+            if (c < p.batch) p.y[(size_t)c * p.n + row] = v[c];
+    } else {
+        const float l = softcap_apply(v[0], p.softcap);
+        if (p.y) p.y[row] = l;
+        if (better(l, (int)row, bv, bi)) {
+            bv = l;
+            bi = (int)row;
+        }
+    }
+}
+
+template <int BITS, int BC, int EPI, int LOG2NB>
+__global__ void __launch_bounds__(256, BC == 1 ? 2 : 1) gemv_stream_kernel(StreamParams p) {
+    using SL = Slot<BITS>;
+    constexpr int NB = 1 << LOG2NB;
+    constexpr int R = NB >= SBW ? 1 : SBW / NB;       // rows per stage
+    constexpr int PARTS = NB > SBW ? NB / SBW : 1;    // stages per row
+    constexpr int NXB = NB >= 32 ? (NB < SBW ? NB / 32 : 8) : 1;  // distinct activation blocks per lane
+    constexpr bool XREG = NB <= 128 && BC * NXB <= 8;  // activation words in registers
+    constexpr int NXR = XREG ? NXB : 1;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = blockDim.x >> 5;
+    const int D = p.stages;  // slots per warp
+
+    // shared layout: slots[W][D] | full[W][D] | xq columns (16-byte aligned)
+    unsigned char* slots = smem + (size_t)warp * D * SL::BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)W * D * SL::BYTES) + warp * D;
+    unsigned char* xqbase = smem + xq_offset(W * D, SL::BYTES);
+    const int xstride = xq_stride(NB);
+
+    const long long r0 = (long long)blockIdx.x * p.n / gridDim.x;
+    const long long r1 = (long long)(blockIdx.x + 1) * p.n / gridDim.x;
+    const int nrows = (int)(r1 - r0);
+    const int nunits = NB >= SBW ? nrows : (nrows + R - 1) / R;      // unit: R rows, or one row
+    const int my_units = nunits > warp ? (nunits - warp + W - 1) / W : 0;
+    const int my_stages = my_units * PARTS;
+
+    const uint64_t pol = policy_evict_first();
+    // issue stage t of this warp (unit warp + W*(t/PARTS), part t%PARTS) into slot t%D
+    auto issue = [&](int t) {
+        const int u = warp + W * (t / PARTS);
+        const int part = t % PARTS;
+        const long long row = r0 + (long long)u * R;
+        const int rows_u = R == 1 ? 1 : min(R, nrows - u * R);
+        const uint32_t blocks = (uint32_t)(NB >= SBW ? SBW : rows_u * NB);
+        const size_t blk0 = (size_t)row * NB + (size_t)part * SBW;  // first block in the matrix
+        unsigned char* st = slots + (size_t)(t % D) * SL::BYTES;
+        uint64_t* bar = &full[t % D];
+        mbar_arrive_expect_tx(bar, blocks * SL::BPB);
+        bulk_g2s(st, p.lo + blk0 * 16, blocks * 16, bar, pol);
+        if constexpr (BITS == 6) bulk_g2s(st + SL::HI, p.hi + blk0 * 8, blocks * 8, bar, pol);
+        bulk_g2s(st + SL::SC, p.scale + blk0, blocks * 2, bar, pol);
+        bulk_g2s(st + SL::MN, p.min + blk0, blocks * 2, bar, pol);
+    };
+
+    if (lane == 0) {
+        pdl_launch_dependents();
+        for (int s = 0; s < D; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+        for (int t = 0; t < D && t < my_stages; ++t) issue(t);
+    }
+    __syncwarp();
+
+    // ---- activation prologue (after the preceding kernel, which may have written x)
+    pdl_wait();
+    for (int c = 0; c < p.batch; ++c)
+        quantize_x_coop<256>(p.x + (size_t)c * p.k, p.k, xq_view(xqbase + c * xstride, NB), threadIdx.x);
+    __syncthreads();
+
+    uint4 xl[BC][NXR], xh[BC][NXR];
+    float xs[BC][NXR], xS[BC][NXR];
+    if constexpr (XREG) {
+#pragma unroll
+        for (int j = 0; j < NXR; ++j) {
+            const int blk = NB >= 32 ? lane + 32 * j : (lane & (NB - 1));
+#pragma unroll
+            for (int c = 0; c < BC; ++c) {
+                const XqView v = xq_view(xqbase + c * xstride, NB);
+                const bool ok = c < p.batch;
+                xl[c][j] = ok ? *reinterpret_cast<const uint4*>(v.lo + 16 * blk) : make_uint4(0, 0, 0, 0);
+                xh[c][j] = ok ? *reinterpret_cast<const uint4*>(v.hi + 16 * blk) : make_uint4(0, 0, 0, 0);
+                xs[c][j] = ok ? v.s[blk] : 0.0f;
+                xS[c][j] = ok ? v.S[blk] : 0.0f;
+            }
+        }
+    }
+
+    float bv = __int_as_float(0x7fc00000);
+    int bi = 0x7fffffff;
+    float rowacc[BC];  // running sum of a row that spans several stages
+#pragma unroll
+    for (int c = 0; c < BC; ++c) rowacc[c] = 0.0f;
+
+    for (int t = 0; t < my_stages; ++t) {
+        const int slot = t % D;
+        if (!mbar_wait(&full[slot], (uint32_t)((t / D) & 1))) {
+            atomicOr(p.err, ERR_WAIT_FULL);
+            break;
+        }
+        const int u = warp + W * (t / PARTS);
+        const int part = t % PARTS;
+        const long long row0 = r0 + (long long)u * R;
+        const int rows_u = R == 1 ? 1 : min(R, nrows - u * R);
+        const unsigned char* st = slots + (size_t)slot * SL::BYTES;
+
+        // stage -> registers
+        uint4 cw[JPL];
+        uint2 hw[JPL];
+        unsigned short dh[JPL], mh[JPL];
+#pragma unroll
+        for (int j = 0; j < JPL; ++j) {
+            const int fb = lane + 32 * j;
+            cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
+            if constexpr (BITS == 6) hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+            dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
+            mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
+        }
+        __syncwarp();
+        if (lane == 0 && t + D < my_stages) {
+            fence_proxy_async();  // the slot's generic reads are done before the async refill
+            issue(t + D);
+        }
+
+        // block partials: part j of the lane belongs to row (lane + 32j) / NB of the stage
+        float pj[BC][JPL];
+#pragma unroll
+        for (int j = 0; j < JPL; ++j) {
+            const int rloc = (NB >= SBW) ? 0 : ((lane + 32 * j) >> LOG2NB);
+            Codes32 cc;
+            if constexpr (BITS == 4)
+                cc = unpack_q4(cw[j]);
+            else
+                cc = unpack_q6(cw[j], hw[j]);
+            const float d = half_bits_to_float(dh[j]);
+            const float m = half_bits_to_float(mh[j]);
+            const bool valid = rloc < rows_u;
+#pragma unroll
+            for (int c = 0; c < BC; ++c) {
+                float r;
+                if constexpr (XREG) {
+                    const int xj = NB >= 32 ? (j % NXR) : 0;
+                    r = block_combine(block_dot(cc, xl[c][xj], xh[c][xj]), d, m, xs[c][xj], xS[c][xj]);
+                } else {
+                    const int blk = (part * SBW + lane + 32 * j) & (NB - 1);
+                    const XqView v = xq_view(xqbase + c * xstride, NB);
+                    const uint4 a = *reinterpret_cast<const uint4*>(v.lo + 16 * blk);
+                    const uint4 b = *reinterpret_cast<const uint4*>(v.hi + 16 * blk);
+                    r = block_combine(block_dot(cc, a, b), d, m, v.s[blk], v.S[blk]);
+                }
+                pj[c][j] = valid ? r : 0.0f;
+            }
+        }
+
+        if constexpr (NB >= 32) {
+            // R rows per stage, JPL/R consecutive j per row
+            constexpr int JR = JPL / R;
+#pragma unroll
+            for (int c = 0; c < BC; ++c) {
+                float rs[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float s = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < JR; ++q) s += pj[c][r * JR + q];
+                    rs[r] = s;
+                }
+                if constexpr (PARTS > 1) {
+                    rowacc[c] += rs[0];
+                    if (part == PARTS - 1) {
+                        float one[1] = {rowacc[c]};
+                        halving_reduce<1, 5>(one);
+                        pj[c][0] = one[0];
+                        rowacc[c] = 0.0f;
+                    }
+                } else {
+                    halving_reduce<R, 5>(rs);
+                    pj[c][0] = rs[0];
+                }
+            }
+            if (PARTS == 1 || part == PARTS - 1) {
+                constexpr int LANES_PER_ROW = 32 / R;
+                if ((lane & (LANES_PER_ROW - 1)) == 0) {
+                    const int r = lane / LANES_PER_ROW;
+                    if (r < rows_u) {
+                        float out[BC];
+#pragma unroll
+                        for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
+                        emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+                    }
+                }
+            }
+        } else {
+            // NB < 32: value j of lane l is row j*(32/NB) + l/NB, summed over NB-lane segments
+#pragma unroll
+            for (int c = 0; c < BC; ++c) halving_reduce<JPL, LOG2NB>(pj[c]);
+            constexpr int KEEP = NB / JPL;  // lanes holding the same value after the halving steps
+            if ((lane & (KEEP - 1)) == 0) {
+                const int v = (lane & (NB - 1)) / KEEP;
+                const int r = v * (32 / NB) + lane / NB;
+                if (r < rows_u) {
+                    float out[BC];
+#pragma unroll
+                    for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
+                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+                }
+            }
+        }
+    }
+
+    if constexpr (EPI == EPI_ARGMAX) {
+        __shared__ ArgmaxPartial sred[8];
+        __shared__ int sflag;
+        argmax_finish(bv, bi, p.ws, p.argmax, sred, &sflag);
+    }
+}
+
+}  // namespace stream
+
+// host launcher for one format (defined in gemv_stream_q4.cu / gemv_stream_q6.cu)
+template <int BITS>
+int launch_stream_bits(const StreamParams& p, int epi, const LaunchCtx& lc);
+
+}  // namespace qg

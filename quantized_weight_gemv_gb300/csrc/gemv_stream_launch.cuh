@@ -1,0 +1,75 @@
+// Host-side choice of ring depth and grid for the streaming GEMV, per format.
+#pragma once
+
+#include <cstdlib>
+
+#include "gemv_stream.cuh"
+
+namespace qg {
+namespace stream {
+
+inline int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    return atoi(v);
+}
+
+template <int BITS, int BC, int EPI, int L>
+int launch_t(StreamParams p, const LaunchCtx& lc) {
+    using SL = Slot<BITS>;
+    auto kern = gemv_stream_kernel<BITS, BC, EPI, L>;
+    constexpr int NB = 1 << L;
+    constexpr int W = 8;  // warps per CTA
+    const size_t fixed = (size_t)BC * xq_stride(NB);
+    // slots per warp: QG_STREAM_SMEM_KB of shared memory per CTA (default 110 KB, so
+    // that CTAs of two consecutive launches can share an SM under PDL), at least 1
+    const long long budget = (long long)env_int("QG_STREAM_SMEM_KB", 110) * 1024;
+    int D = env_int("QG_STREAM_SLOTS", 0);
+    if (D <= 0) D = (int)((budget - (long long)fixed - 16) / ((long long)W * (SL::BYTES + 8)));
+    if (D < 1) D = 1;
+    if (D > 8) D = 8;
+    const size_t cap = (size_t)lc.max_smem_optin - 1024;  // room for static shared memory
+    size_t smem = xq_offset(W * D, SL::BYTES) + fixed;
+    while (smem > cap && D > 1) {
+        --D;
+        smem = xq_offset(W * D, SL::BYTES) + fixed;
+    }
+    if (smem > cap) return QG_ERR_UNSUPPORTED;
+    if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
+    p.stages = D;
+    p.err = lc.err;
+    int per_sm = env_int("QG_STREAM_CTAS_PER_SM", 1);
+    if (per_sm < 1) per_sm = 1;
+    int grid = lc.sm_count * per_sm;
+    if (EPI == EPI_ARGMAX && grid > VOCAB_MAX_CTAS) grid = VOCAB_MAX_CTAS;
+    if (grid > p.n) grid = p.n;
+    if (grid < 1) grid = 1;
+    return launch_kernel(kern, dim3(grid), dim3(W * 32), smem, lc, p);
+}
+
+template <int BITS, int BC, int EPI>
+int launch_l(const StreamParams& p, const LaunchCtx& lc) {
+    switch (p.log2nb) {
+        case 3: return launch_t<BITS, BC, EPI, 3>(p, lc);
+        case 4: return launch_t<BITS, BC, EPI, 4>(p, lc);
+        case 5: return launch_t<BITS, BC, EPI, 5>(p, lc);
+        case 6: return launch_t<BITS, BC, EPI, 6>(p, lc);
+        case 7: return launch_t<BITS, BC, EPI, 7>(p, lc);
+        case 8: return launch_t<BITS, BC, EPI, 8>(p, lc);
+        case 9: return launch_t<BITS, BC, EPI, 9>(p, lc);
+    }
+    return QG_ERR_UNSUPPORTED;
+}
+
+template <int BITS>
+int launch_bits(const StreamParams& p, int epi, const LaunchCtx& lc) {
+    if (epi == EPI_ARGMAX) return launch_l<BITS, 1, EPI_ARGMAX>(p, lc);
+    switch (p.batch) {
+        case 1: return launch_l<BITS, 1, EPI_STORE>(p, lc);
+        case 2: return launch_l<BITS, 2, EPI_STORE>(p, lc);
+        default: return launch_l<BITS, 4, EPI_STORE>(p, lc);
+    }
+}
+
+}  // namespace stream
+}  // namespace qg

@@ -1,0 +1,9 @@
+// Streaming GEMV instantiations for 6-bit weights.
+#include "gemv_stream_launch.cuh"
+
+namespace qg {
+template <>
+int launch_stream_bits<6>(const StreamParams& p, int epi, const LaunchCtx& lc) {
+    return stream::launch_bits<6>(p, epi, lc);
+}
+}  // namespace qg

@@ -150,6 +150,39 @@ int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const u
                          size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * Grouped GEMV: `count` independent GEMVs of one weight format in two launches
+ * (needle.js "Inference backends", "Hybrid GPU execution": independent projections
+ * batched into one dispatch over a combined weight arena; genie-ai-runtime,
+ * "v1.2.0": a QKV GEMV sharing one q8_1 activation).  Each descriptor computes
+ * y = GEMV(weights, x) exactly as qgemv_q4/qgemv_q6 define it.
+ *   descs : HOST array of `count` descriptors, read during the call only (they are
+ *           copied into the kernel parameters); the pointers inside are device
+ *           pointers; hi is NULL for bits == 4.
+ *   0 <= count <= QG_MAX_GROUP; for every descriptor n >= 0 and k a power of two
+ *           with 1024 <= k <= 16384.  Descriptors may share x; outputs must not overlap.
+ *   ws    : device workspace of at least qg_grouped_workspace_bytes(descs, count)
+ *           bytes (the quantised activations), 16-byte aligned, no initial content.
+ * The second launch is always chained to the first by programmatic dependent
+ * launch; QG_FLAG_PDL applies to the first.
+ */
+typedef struct qg_gemv_desc {
+    const uint8_t* lo;     /* Q4 codes, or the Q6 low planes */
+    const uint8_t* hi;     /* Q6 high planes; NULL for Q4 */
+    const uint16_t* scale; /* binary16 [n][k/32] */
+    const uint16_t* min;   /* binary16 [n][k/32] */
+    const float* x;        /* [k] */
+    float* y;              /* [n] */
+    int n;
+    int k;
+} qg_gemv_desc;
+
+#define QG_MAX_GROUP 256
+
+size_t qg_grouped_workspace_bytes(const qg_gemv_desc* descs, int count);
+int qgemv_grouped(int bits, const qg_gemv_desc* descs, int count, void* ws, size_t ws_bytes, unsigned flags,
+                  void* stream);
+
+/*
  * Exposed steps, for exactness checks of the integer parts.
  * qg_quantize_act: per-block int8 quantisation of `batch` rows of x [batch][k]:
  *   xq int8 [batch][k], xs fp32 [batch][k/32] (s_b), xsum int32 [batch][k/32] (sum of xq).

@@ -39,6 +39,8 @@ SIGNATURES = {
     "cq_fwht_matvec": (_i, [_u8p, _u16p, _u16p, _i, _i, _i, _i, _i, _f32p, _f32p, _u, _vp]),
     "qg_vocab_workspace_bytes": (_sz, []),
     "vocab_softcap_argmax": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _f32p, _f, _f32p, _i32p, _vp, _sz, _u, _vp]),
+    "qg_grouped_workspace_bytes": (_sz, [_vp, _i]),
+    "qgemv_grouped": (_i, [_i, _vp, _i, _vp, _sz, _u, _vp]),
     "qg_quantize_act": (_i, [_f32p, _i, _i, _i8p, _f32p, _i32p, _vp]),
     "qg_blockdots": (_i, [_i, _u8p, _u8p, _i, _i, _i8p, _i32p, _vp]),
 }
@@ -217,6 +219,63 @@ def vocab_softcap_argmax(bits, lo, hi, scale, min, x, softcap: float = 30.0, log
                                           ws.numel() * ws.element_size(), flags, _stream(dev)),
                "vocab_softcap_argmax")
     return logits, argmax
+
+
+class GemvDesc(ctypes.Structure):
+    """Mirror of ``qg_gemv_desc``."""
+    _fields_ = [("lo", ctypes.c_void_p), ("hi", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("min", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("n", ctypes.c_int), ("k", ctypes.c_int)]
+
+
+QG_MAX_GROUP = 256
+
+
+class GroupedGemv:
+    """A fixed list of independent GEMVs (one weight format) run by :func:`qgemv_grouped`.
+
+    ``mats``: weight dicts with device tensors ("lo", ["hi"], "scale", "min");
+    ``xs``/``ys``: matching device activations [k] and outputs [n].  The descriptor
+    array and the workspace are built once; ``run()`` enqueues the two launches.
+    """
+
+    def __init__(self, bits, mats, xs, ys, flags: int = 0):
+        if not 0 < len(mats) <= QG_MAX_GROUP or len(mats) != len(xs) or len(mats) != len(ys):
+            raise ValueError("need 1..256 matching weights, activations and outputs")
+        self.bits = bits
+        self.flags = flags
+        dev = mats[0]["lo"].device
+        for m, x, y in zip(mats, xs, ys):
+            _need(m["lo"], "lo", _U8, dev)
+            if bits == 6:
+                _need(m["hi"], "hi", _U8, dev)
+            _need(m["scale"], "scale", _H16, dev)
+            _need(m["min"], "min", _H16, dev)
+            _need(x, "x", _F32, dev)
+            _need(y, "y", _F32, dev)
+        self.keep = (mats, xs, ys)  # the descriptors hold raw pointers into these tensors
+        arr = (GemvDesc * len(mats))()
+        for i, (m, x, y) in enumerate(zip(mats, xs, ys)):
+            arr[i] = GemvDesc(m["lo"].data_ptr(), m["hi"].data_ptr() if bits == 6 else None,
+                              m["scale"].data_ptr(), m["min"].data_ptr(), x.data_ptr(), y.data_ptr(),
+                              m["lo"].shape[0], m["lo"].shape[1] * 2)
+        self.descs = arr
+        self.count = len(mats)
+        self.device = dev
+        nbytes = int(lib().qg_grouped_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), self.count))
+        self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+
+    def run(self):
+        with torch.cuda.device(self.device):
+            _check(lib().qgemv_grouped(self.bits, ctypes.cast(self.descs, ctypes.c_void_p), self.count,
+                                       _ptr(self.ws), self.ws.numel(), self.flags, _stream(self.device)),
+                   "qgemv_grouped")
+
+
+def qgemv_grouped(bits, mats, xs, ys, flags: int = 0):
+    """One-shot :class:`GroupedGemv` call; returns ``ys``."""
+    GroupedGemv(bits, mats, xs, ys, flags).run()
+    return ys
 
 
 def qg_quantize_act(x):

@@ -207,6 +207,38 @@ int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const u
     return launch_plain(pp, bits, EPI_ARGMAX, lc);
 }
 
+size_t qg_grouped_workspace_bytes(const qg_gemv_desc* descs, int count) {
+    if (!descs || count <= 0 || count > QG_MAX_GROUP) return 0;
+    return grouped_workspace_bytes(descs, count);
+}
+
+int qgemv_grouped(int bits, const qg_gemv_desc* descs, int count, void* ws, size_t ws_bytes, unsigned flags,
+                  void* stream) {
+    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
+    if (count < 0 || count > QG_MAX_GROUP) return QG_ERR_INVALID_ARG;
+    if (count == 0) return QG_OK;
+    if (!descs) return QG_ERR_INVALID_ARG;
+    int active = 0;
+    for (int i = 0; i < count; ++i) {
+        const qg_gemv_desc& d = descs[i];
+        if (d.n < 0) return QG_ERR_INVALID_ARG;
+        if (d.k < 1024 || d.k > 16384 || (d.k & (d.k - 1)) != 0) return QG_ERR_UNSUPPORTED;
+        if (d.n == 0) continue;
+        int rc = check_weights(bits, d.lo, d.hi, d.scale, d.min, d.n, d.k);
+        if (rc != QG_OK) return rc;
+        if (!d.x || !d.y) return QG_ERR_INVALID_ARG;
+        if (!aligned16(d.x) || !aligned16(d.y)) return QG_ERR_ALIGNMENT;
+        ++active;
+    }
+    if (active == 0) return QG_OK;
+    if (!ws || ws_bytes < grouped_workspace_bytes(descs, count)) return QG_ERR_WORKSPACE;
+    if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    int rc = resolve(stream, flags, lc);
+    if (rc != QG_OK) return rc;
+    return launch_grouped(bits, descs, count, reinterpret_cast<unsigned char*>(ws), lc);
+}
+
 int qg_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, void* stream) {
     if (k <= 0 || (k & 31) != 0 || k > QG_MAX_K || batch < 1 || batch > QG_MAX_BATCH) return QG_ERR_INVALID_ARG;
     if (!x || !xq || !xs || !xsum) return QG_ERR_INVALID_ARG;

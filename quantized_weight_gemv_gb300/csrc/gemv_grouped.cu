@@ -1,0 +1,381 @@
+// Grouped GEMV: many independent quantized-weight GEMVs in two launches.
+//
+// needle.js "Inference backends", "Hybrid GPU execution": independent projections
+// go through matvecBatch, their packed weights combined so that one dispatch covers
+// the whole group; genie-ai-runtime "v1.2.0": a triple QKV GEMV sharing one q8_1
+// activation.  Here the group is a list of up to QG_MAX_GROUP descriptors (weights,
+// x, y, n, k), passed by value as the kernel parameter, so nothing is allocated:
+//  1. grouped_quantize_kernel: every activation of the group, quantised per block
+//     of 32 (one warp per block) into the caller's workspace;
+//  2. grouped_gemv_kernel (programmatic dependent launch on 1): persistent CTAs
+//     split the concatenated work of all descriptors - units of 256 blocks (whole
+//     rows), or single rows of k/8192 such units for k > 8192 - into contiguous,
+//     equal shares of bulk-copy stages.  Each warp streams its units through a
+//     private ring exactly as the single-matrix streaming kernel does; the ring
+//     starts filling before griddepcontrol.wait, i.e. while kernel 1 still runs.
+#include <cstring>
+
+#include "gemv_stream.cuh"
+
+namespace qg {
+namespace grouped {
+
+using stream::SBW;
+using stream::JPL;
+
+struct GDesc {
+    const uint8_t* lo;
+    const uint8_t* hi;
+    const uint16_t* scale;
+    const uint16_t* min;
+    const float* x;
+    float* y;
+    int n;
+    int log2nb;        // log2(k / 32), 5..9
+    int units;         // work units of this descriptor
+    int parts;         // stages per unit (1, or nb / 256)
+    int unit_prefix;   // units of the descriptors before
+    int stage_prefix;  // stages of the descriptors before
+    int qb_prefix;     // activation blocks of the descriptors before
+    int ws_off;        // byte offset of this descriptor's activation image in the workspace
+};
+
+struct GParams {
+    int count;
+    int total_units;
+    int total_stages;
+    int total_qblocks;
+    int stages_per_warp;
+    unsigned int* err;
+    unsigned char* ws;
+    GDesc d[QG_MAX_GROUP];
+};
+
+// descriptor holding global index v of a prefix array (largest d with prefix <= v)
+template <typename F>
+__device__ __forceinline__ int find_desc(const GParams& p, int v, F prefix) {
+    int lo = 0, hi = p.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix(p.d[mid]) <= v)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(256) grouped_quantize_kernel(const __grid_constant__ GParams p) {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    for (int g = blockIdx.x * 8 + (threadIdx.x >> 5); g < p.total_qblocks; g += gridDim.x * 8) {
+        const int di = find_desc(p, g, [](const GDesc& d) { return d.qb_prefix; });
+        const GDesc& d = p.d[di];
+        const int b = g - d.qb_prefix;
+        const int nb = 1 << d.log2nb;
+        float s;
+        int S;
+        const int q = quantize_lane(d.x[32 * b + lane], s, S);
+        const XqView v = xq_view(p.ws + d.ws_off, nb);
+        if (lane < 16)
+            v.lo[16 * b + lane] = (int8_t)q;
+        else
+            v.hi[16 * b + lane - 16] = (int8_t)q;
+        if (lane == 0) {
+            v.s[b] = s;
+            v.S[b] = (float)S;
+        }
+    }
+}
+
+// Walks one warp's units: w, w+8, ... of the CTA's unit range, part by part.
+struct Cursor {
+    int g;     // global unit
+    int part;  // stage within the unit
+    int d;     // descriptor of g
+    __device__ __forceinline__ void advance(const GParams& p) {
+        if (++part == p.d[d].parts) {
+            part = 0;
+            g += 8;
+            while (d + 1 < p.count && g >= p.d[d + 1].unit_prefix) ++d;
+        }
+    }
+};
+
+// first global unit whose first stage is at or after global stage x
+__device__ __forceinline__ int unit_at_stage(const GParams& p, int x) {
+    if (x >= p.total_stages) return p.total_units;
+    const int di = find_desc(p, x, [](const GDesc& d) { return d.stage_prefix; });
+    const GDesc& d = p.d[di];
+    const int local = (x - d.stage_prefix + d.parts - 1) / d.parts;
+    return d.unit_prefix + local;
+}
+
+template <int BITS, int L>
+__device__ __forceinline__ void stage_compute(const GDesc& d, const unsigned char* xqws, int unit_local, int part,
+                                              const uint4 (&cw)[JPL], const uint2 (&hw)[JPL],
+                                              const unsigned short (&dh)[JPL], const unsigned short (&mh)[JPL],
+                                              const uint4 (&xl)[2], const uint4 (&xh)[2], const float (&xs)[2],
+                                              const float (&xS)[2], float& rowacc) {
+    constexpr int NB = 1 << L;
+    constexpr int R = NB >= SBW ? 1 : SBW / NB;
+    constexpr int PARTS = NB > SBW ? NB / SBW : 1;
+    constexpr bool XREG = NB <= 64;
+    const int lane = threadIdx.x & 31;
+    const long long row0 = (long long)unit_local * R;
+    const int rows_u = R == 1 ? 1 : min(R, d.n - unit_local * R);
+    const XqView v = xq_view(const_cast<unsigned char*>(xqws), NB);
+
+    float pj[JPL];
+#pragma unroll
+    for (int j = 0; j < JPL; ++j) {
+        const int rloc = (NB >= SBW) ? 0 : ((lane + 32 * j) >> L);
+        Codes32 cc;
+        if constexpr (BITS == 4)
+            cc = unpack_q4(cw[j]);
+        else
+            cc = unpack_q6(cw[j], hw[j]);
+        const float dd = half_bits_to_float(dh[j]);
+        const float mm = half_bits_to_float(mh[j]);
+        float r;
+        if constexpr (XREG) {
+            const int xj = j % (NB / 32);
+            r = block_combine(block_dot(cc, xl[xj], xh[xj]), dd, mm, xs[xj], xS[xj]);
+        } else {
+            const int blk = (part * SBW + lane + 32 * j) & (NB - 1);
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(v.lo + 16 * blk));
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(v.hi + 16 * blk));
+            r = block_combine(block_dot(cc, a, b), dd, mm, __ldg(v.s + blk), __ldg(v.S + blk));
+        }
+        pj[j] = rloc < rows_u ? r : 0.0f;
+    }
+    constexpr int JR = JPL / R;
+    float rs[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float s = 0.0f;
+#pragma unroll
+        for (int q = 0; q < JR; ++q) s += pj[r * JR + q];
+        rs[r] = s;
+    }
+    if constexpr (PARTS > 1) {
+        rowacc += rs[0];
+        if (part != PARTS - 1) return;
+        rs[0] = rowacc;
+        rowacc = 0.0f;
+    }
+    stream::halving_reduce<R, 5>(rs);
+    constexpr int LPR = 32 / R;
+    if ((lane & (LPR - 1)) == 0) {
+        const int r = lane / LPR;
+        if (r < rows_u) d.y[row0 + r] = rs[0];
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(256, 1) grouped_gemv_kernel(const __grid_constant__ GParams p) {
+    using SL = stream::Slot<BITS>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = p.stages_per_warp;
+    unsigned char* slots = smem + (size_t)warp * D * SL::BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)8 * D * SL::BYTES) + warp * D;
+
+    // this CTA's units: those whose first stage lies in its equal share of all stages
+    const long long T = p.total_stages;
+    const int u_begin = unit_at_stage(p, (int)(T * blockIdx.x / gridDim.x));
+    const int u_end = unit_at_stage(p, (int)(T * (blockIdx.x + 1) / gridDim.x));
+
+    Cursor ic, cc;  // issue and consume cursors
+    ic.g = u_begin + warp;
+    ic.part = 0;
+    ic.d = ic.g < p.total_units ? find_desc(p, ic.g, [](const GDesc& d) { return d.unit_prefix; }) : 0;
+    cc = ic;
+
+    const uint64_t pol = stream::policy_evict_first();
+    auto issue = [&](int t) {  // stage at cursor ic into slot t % D
+        const GDesc& d = p.d[ic.d];
+        const int nb = 1 << d.log2nb;
+        const int R = nb >= SBW ? 1 : SBW / nb;
+        const int ul = ic.g - d.unit_prefix;
+        const int rows_u = R == 1 ? 1 : min(R, d.n - ul * R);
+        const uint32_t blocks = (uint32_t)(nb >= SBW ? SBW : rows_u * nb);
+        const size_t blk0 = (size_t)ul * R * nb + (size_t)ic.part * SBW;
+        unsigned char* st = slots + (size_t)(t % D) * SL::BYTES;
+        uint64_t* bar = &full[t % D];
+        stream::mbar_arrive_expect_tx(bar, blocks * SL::BPB);
+        stream::bulk_g2s(st, d.lo + blk0 * 16, blocks * 16, bar, pol);
+        if constexpr (BITS == 6) stream::bulk_g2s(st + SL::HI, d.hi + blk0 * 8, blocks * 8, bar, pol);
+        stream::bulk_g2s(st + SL::SC, d.scale + blk0, blocks * 2, bar, pol);
+        stream::bulk_g2s(st + SL::MN, d.min + blk0, blocks * 2, bar, pol);
+    };
+
+    int issued = 0;
+    if (lane == 0) {
+        pdl_launch_dependents();
+        for (int s = 0; s < D; ++s) stream::mbar_init(&full[s], 1);
+        stream::fence_mbar_init();
+        while (issued < D && ic.g < u_end) {
+            issue(issued);
+            ++issued;
+            ic.advance(p);
+        }
+    }
+    __syncwarp();
+    pdl_wait();  // the activation images and the outputs depend on the preceding kernel
+
+    uint4 xl[2], xh[2];
+    float xs[2], xS[2];
+    int xd = -1;  // descriptor whose activation words are in registers
+    float rowacc = 0.0f;
+
+    for (int t = 0; cc.g < u_end; ++t) {
+        const int slot = t % D;
+        if (!stream::mbar_wait(&full[slot], (uint32_t)((t / D) & 1))) {
+            atomicOr(p.err, ERR_WAIT_FULL);
+            break;
+        }
+        const unsigned char* st = slots + (size_t)slot * SL::BYTES;
+        uint4 cw[JPL];
+        uint2 hw[JPL];
+        unsigned short dh[JPL], mh[JPL];
+#pragma unroll
+        for (int j = 0; j < JPL; ++j) {
+            const int fb = lane + 32 * j;
+            cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
+            if constexpr (BITS == 6) hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+            dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
+            mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
+        }
+        __syncwarp();
+        if (lane == 0 && ic.g < u_end) {
+            stream::fence_proxy_async();
+            issue(t + D);
+            ic.advance(p);
+        }
+
+        const GDesc& d = p.d[cc.d];
+        const unsigned char* xqws = p.ws + d.ws_off;
+        if (d.log2nb <= 6 && xd != cc.d) {  // activation words of a new descriptor
+            const int nb = 1 << d.log2nb;
+            const XqView v = xq_view(const_cast<unsigned char*>(xqws), nb);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int blk = min(lane + 32 * j, nb - 1);
+                xl[j] = __ldg(reinterpret_cast<const uint4*>(v.lo + 16 * blk));
+                xh[j] = __ldg(reinterpret_cast<const uint4*>(v.hi + 16 * blk));
+                xs[j] = __ldg(v.s + blk);
+                xS[j] = __ldg(v.S + blk);
+            }
+            xd = cc.d;
+        }
+        const int ul = cc.g - d.unit_prefix;
+        switch (d.log2nb) {
+            case 5:
+                stage_compute<BITS, 5>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                break;
+            case 6:
+                stage_compute<BITS, 6>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                break;
+            case 7:
+                stage_compute<BITS, 7>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                break;
+            case 8:
+                stage_compute<BITS, 8>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                break;
+            default:
+                stage_compute<BITS, 9>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                break;
+        }
+        cc.advance(p);
+    }
+}
+
+static int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    return atoi(v);
+}
+
+}  // namespace grouped
+
+size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count) {
+    size_t off = 0;
+    for (int i = 0; i < count; ++i) off += (size_t)xq_stride(descs[i].k >> 5);
+    return off;
+}
+
+int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc) {
+    using namespace grouped;
+    static_assert(sizeof(GParams) < 32000, "grouped parameters must fit the kernel parameter space");
+    GParams p;
+    memset(&p, 0, sizeof(p));
+    long long units = 0, stages = 0, qblocks = 0, off = 0;
+    int m = 0;
+    for (int i = 0; i < count; ++i) {
+        const qg_gemv_desc& s = descs[i];
+        if (s.n == 0) continue;
+        const int nb = s.k >> 5;
+        int l = 0;
+        while ((1 << l) < nb) ++l;
+        GDesc& d = p.d[m++];
+        d.lo = s.lo;
+        d.hi = s.hi;
+        d.scale = s.scale;
+        d.min = s.min;
+        d.x = s.x;
+        d.y = s.y;
+        d.n = s.n;
+        d.log2nb = l;
+        const int R = nb >= 256 ? 1 : 256 / nb;
+        d.parts = nb > 256 ? nb / 256 : 1;
+        d.units = nb >= 256 ? s.n : (s.n + R - 1) / R;
+        d.unit_prefix = (int)units;
+        d.stage_prefix = (int)stages;
+        d.qb_prefix = (int)qblocks;
+        d.ws_off = (int)off;
+        units += d.units;
+        stages += (long long)d.units * d.parts;
+        qblocks += nb;
+        off += xq_stride(nb);
+    }
+    if (m == 0) return QG_OK;
+    if (stages > 0x7fffffffLL || off > 0x7fffffffLL) return QG_ERR_UNSUPPORTED;
+    p.count = m;
+    p.total_units = (int)units;
+    p.total_stages = (int)stages;
+    p.total_qblocks = (int)qblocks;
+    p.err = lc.err;
+    p.ws = ws;
+
+    // 1. activations
+    long long qgrid = (qblocks + 7) / 8;
+    if (qgrid > lc.sm_count * 16) qgrid = lc.sm_count * 16;
+    int rc = launch_kernel(grouped_quantize_kernel, dim3((unsigned)qgrid), dim3(256), 0, lc, p);
+    if (rc != QG_OK) return rc;
+
+    // 2. the GEMVs, always chained to 1 by programmatic dependent launch
+    const int slot = (bits == 4 ? stream::Slot<4>::BYTES : stream::Slot<6>::BYTES) + 8;
+    const long long budget = (long long)env_int("QG_GROUPED_SMEM_KB", 200) * 1024;
+    int D = env_int("QG_GROUPED_SLOTS", 0);
+    if (D <= 0) D = (int)(budget / (8LL * slot));
+    if (D < 1) D = 1;
+    if (D > 16) D = 16;
+    const size_t cap = (size_t)lc.max_smem_optin - 1024;
+    while ((size_t)8 * D * slot > cap && D > 1) --D;
+    const size_t smem = (size_t)8 * D * slot;
+    p.stages_per_warp = D;
+    const void* kern = bits == 4 ? (const void*)grouped_gemv_kernel<4> : (const void*)grouped_gemv_kernel<6>;
+    if (int e = ensure_smem_attr(kern, smem, lc)) return e;
+    int per_sm = env_int("QG_GROUPED_CTAS_PER_SM", 1);
+    if (per_sm < 1) per_sm = 1;
+    long long grid = (long long)lc.sm_count * per_sm;
+    if (grid > units) grid = units;
+    LaunchCtx lc2 = lc;
+    lc2.flags |= QG_FLAG_PDL;
+    if (bits == 4) return launch_kernel(grouped_gemv_kernel<4>, dim3((unsigned)grid), dim3(256), smem, lc2, p);
+    return launch_kernel(grouped_gemv_kernel<6>, dim3((unsigned)grid), dim3(256), smem, lc2, p);
+}
+
+}  // namespace qg

@@ -120,3 +120,29 @@ def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError):
         qg.qgemv_q4(t, torch.zeros(4, 1, dtype=torch.float16), torch.zeros(4, 1, dtype=torch.float16),
                     torch.zeros(64))
+
+
+def test_grouped_validation(lib):
+    D = qg.GemvDesc
+    ok = D(0x10000, None, 0x10000, 0x10000, 0x10000, 0x10000, 8, 2048)
+    arr = (D * 2)(ok, ok)
+    vp = ctypes.cast(arr, ctypes.c_void_p)
+    need = lib.qg_grouped_workspace_bytes(vp, 2)
+    assert need == 2 * 40 * 64
+    assert lib.qg_grouped_workspace_bytes(None, 2) == 0
+    f = lib.qgemv_grouped
+    assert f(5, vp, 2, A16, need, 0, None) == qg.QG_ERR_UNSUPPORTED
+    assert f(4, vp, 257, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(4, vp, 0, None, 0, 0, None) == qg.QG_OK
+    assert f(4, None, 2, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(4, vp, 2, None, need, 0, None) == qg.QG_ERR_WORKSPACE
+    assert f(4, vp, 2, A16, need - 1, 0, None) == qg.QG_ERR_WORKSPACE
+    assert f(4, vp, 2, MIS, need, 0, None) == qg.QG_ERR_ALIGNMENT
+    bad = (D * 1)(D(0x10000, None, 0x10000, 0x10000, 0x10000, 0x10000, 8, 1536))
+    assert f(4, ctypes.cast(bad, ctypes.c_void_p), 1, A16, need, 0, None) == qg.QG_ERR_UNSUPPORTED
+    bad = (D * 1)(D(0x10000, None, 0x10000, 0x10000, 0x10004, 0x10000, 8, 2048))
+    assert f(4, ctypes.cast(bad, ctypes.c_void_p), 1, A16, need, 0, None) == qg.QG_ERR_ALIGNMENT
+    bad = (D * 1)(D(0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 8, 2048))  # hi given for Q4
+    assert f(4, ctypes.cast(bad, ctypes.c_void_p), 1, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
+    empty = (D * 1)(D(None, None, None, None, None, None, 0, 2048))
+    assert f(4, ctypes.cast(empty, ctypes.c_void_p), 1, None, 0, 0, None) == qg.QG_OK

@@ -281,3 +281,65 @@ def test_cq_constant_index_closed_form():
     y = qg.cq_fwht_matvec(md["idx"], md["codebook"], md["row_scale"], torch.from_numpy(x).to(DEV), g).cpu().numpy()
     ref = (m["row_scale"].view(np.float16).astype(np.float64) * float(np.float16(cb[7])) * np.sqrt(g) * float(x[0]))
     assert_close(y, ref)
+
+
+# ---------------------------------------------------------------- grouped
+@pytest.mark.parametrize("bits", [4, 6])
+def test_grouped_mixed_shapes(bits):
+    shapes = [(2048, 2048), (1024, 2048), (7, 1024), (0, 2048), (300, 16384), (1, 4096), (513, 8192), (16384, 2048),
+              (33, 1024), (2048, 16384)]
+    mats, xs, ys, ws_np, x_np = [], [], [], [], []
+    shared = datagen.normal_f32(999, 1, 2048)
+    for i, (n, k) in enumerate(shapes):
+        w = datagen.make_quantized(bits, 500 + i, n, k)
+        x = shared if k == 2048 and i % 2 == 0 else datagen.normal_f32(500 + i, 1, k)
+        ws_np.append(w)
+        x_np.append(x)
+        wd = dev_w(w)
+        mats.append(wd)
+        xs.append(torch.from_numpy(x).to(DEV))
+        ys.append(torch.full((n,), float("nan"), device=DEV))
+    for flags in (0, qg.QG_FLAG_PDL):
+        for y in ys:
+            y.fill_(float("nan"))
+        qg.qgemv_grouped(bits, mats, xs, ys, flags=flags)
+        for w, x, y in zip(ws_np, x_np, ys):
+            if w["n"] == 0:
+                continue
+            ref = oracle_gemv_par(w, x) if w["n"] > 2000 else oracle.gemv(w, x)
+            assert_close(y.cpu().numpy().astype(np.float64), ref)
+
+
+def test_grouped_matches_single_calls_and_repeats():
+    """The grouped launch and per-call launches give the same rows; repeated runs are identical."""
+    shapes = [(2048, 2048), (1024, 2048), (1024, 2048), (2048, 2048), (16384, 2048), (16384, 2048), (2048, 16384)]
+    mats, xs, ys = [], [], []
+    for i, (n, k) in enumerate(shapes):
+        w = datagen.make_quantized(4, 1000 + i, n, k)
+        mats.append(dev_w(w))
+        xs.append(torch.from_numpy(datagen.normal_f32(1000 + i, 1, k)).to(DEV))
+        ys.append(torch.empty(n, device=DEV))
+    g = qg.GroupedGemv(4, mats, xs, ys)
+    g.run()
+    first = [y.clone() for y in ys]
+    g.run()
+    for a, b, m, x in zip(first, ys, mats, xs):
+        assert torch.equal(a, b)  # deterministic
+        single = qg.qgemv_q4(m["lo"], m["scale"], m["min"], x)
+        assert oracle.normwise_error(a.cpu().numpy(), single.cpu().numpy()) < 1e-5
+
+
+def test_grouped_many_descriptors():
+    """256 small descriptors (the maximum), each a few rows."""
+    mats, xs, ys, ref = [], [], [], []
+    for i in range(256):
+        n = 1 + (i * 7) % 40
+        w = datagen.make_quantized(4, 2000 + i, n, 1024)
+        x = datagen.normal_f32(2000 + i, 1, 1024)
+        mats.append(dev_w(w))
+        xs.append(torch.from_numpy(x).to(DEV))
+        ys.append(torch.empty(n, device=DEV))
+        ref.append(oracle.gemv(w, x))
+    qg.qgemv_grouped(4, mats, xs, ys)
+    for y, r in zip(ys, ref):
+        assert_close(y.cpu().numpy().astype(np.float64), r)

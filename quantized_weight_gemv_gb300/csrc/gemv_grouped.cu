@@ -131,22 +131,18 @@ __device__ __forceinline__ void stage_compute(const GDesc& d, const unsigned cha
 #pragma unroll
     for (int j = 0; j < JPL; ++j) {
         const int rloc = (NB >= SBW) ? 0 : ((lane + 32 * j) >> L);
-        Codes32 cc;
-        if constexpr (BITS == 4)
-            cc = unpack_q4(cw[j]);
-        else
-            cc = unpack_q6(cw[j], hw[j]);
+
         const float dd = half_bits_to_float(dh[j]);
         const float mm = half_bits_to_float(mh[j]);
         float r;
         if constexpr (XREG) {
             const int xj = j % (NB / 32);
-            r = block_combine(block_dot(cc, xl[xj], xh[xj]), dd, mm, xs[xj], xS[xj]);
+            r = block_combine(qdot<BITS>(cw[j], hw[j], xl[xj], xh[xj]), dd, mm, xs[xj], xS[xj]);
         } else {
             const int blk = (part * SBW + lane + 32 * j) & (NB - 1);
             const uint4 a = __ldg(reinterpret_cast<const uint4*>(v.lo + 16 * blk));
             const uint4 b = __ldg(reinterpret_cast<const uint4*>(v.hi + 16 * blk));
-            r = block_combine(block_dot(cc, a, b), dd, mm, __ldg(v.s + blk), __ldg(v.S + blk));
+            r = block_combine(qdot<BITS>(cw[j], hw[j], a, b), dd, mm, __ldg(v.s + blk), __ldg(v.S + blk));
         }
         pj[j] = rloc < rows_u ? r : 0.0f;
     }
@@ -173,8 +169,8 @@ __device__ __forceinline__ void stage_compute(const GDesc& d, const unsigned cha
     }
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(256, 1) grouped_gemv_kernel(const __grid_constant__ GParams p) {
+template <int BITS, int MINB>
+__global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_constant__ GParams p) {
     using SL = stream::Slot<BITS>;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,7 +240,10 @@ __global__ void __launch_bounds__(256, 1) grouped_gemv_kernel(const __grid_const
         for (int j = 0; j < JPL; ++j) {
             const int fb = lane + 32 * j;
             cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
-            if constexpr (BITS == 6) hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+            if constexpr (BITS == 6)
+                hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+            else
+                hw[j] = make_uint2(0u, 0u);
             dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
             mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
         }
@@ -355,27 +354,39 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
     int rc = launch_kernel(grouped_quantize_kernel, dim3((unsigned)qgrid), dim3(256), 0, lc, p);
     if (rc != QG_OK) return rc;
 
-    // 2. the GEMVs, always chained to 1 by programmatic dependent launch
+    // 2. the GEMVs, always chained to 1 by programmatic dependent launch.  Default:
+    // two CTAs per SM (16 warps, at most 128 registers each) and one ring slot per
+    // warp - measured on GB300 as the fastest shape: the slot is refilled as soon as
+    // it has been copied to registers, so 16 x 5 KB stay in flight per SM.  The
+    // diagnostic switches QG_GROUPED_CTAS_PER_SM (1 or 2) and QG_GROUPED_SLOTS
+    // (slots per warp) override it.
+    int per_sm = env_int("QG_GROUPED_CTAS_PER_SM", 2);
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 2) per_sm = 2;
     const int slot = (bits == 4 ? stream::Slot<4>::BYTES : stream::Slot<6>::BYTES) + 8;
-    const long long budget = (long long)env_int("QG_GROUPED_SMEM_KB", 200) * 1024;
-    int D = env_int("QG_GROUPED_SLOTS", 0);
-    if (D <= 0) D = (int)(budget / (8LL * slot));
+    int D = env_int("QG_GROUPED_SLOTS", 1);
     if (D < 1) D = 1;
     if (D > 16) D = 16;
     const size_t cap = (size_t)lc.max_smem_optin - 1024;
     while ((size_t)8 * D * slot > cap && D > 1) --D;
     const size_t smem = (size_t)8 * D * slot;
     p.stages_per_warp = D;
-    const void* kern = bits == 4 ? (const void*)grouped_gemv_kernel<4> : (const void*)grouped_gemv_kernel<6>;
+    const void* kern;
+    if (bits == 4)
+        kern = per_sm == 1 ? (const void*)grouped_gemv_kernel<4, 1> : (const void*)grouped_gemv_kernel<4, 2>;
+    else
+        kern = per_sm == 1 ? (const void*)grouped_gemv_kernel<6, 1> : (const void*)grouped_gemv_kernel<6, 2>;
     if (int e = ensure_smem_attr(kern, smem, lc)) return e;
-    int per_sm = env_int("QG_GROUPED_CTAS_PER_SM", 1);
-    if (per_sm < 1) per_sm = 1;
     long long grid = (long long)lc.sm_count * per_sm;
     if (grid > units) grid = units;
     LaunchCtx lc2 = lc;
     lc2.flags |= QG_FLAG_PDL;
-    if (bits == 4) return launch_kernel(grouped_gemv_kernel<4>, dim3((unsigned)grid), dim3(256), smem, lc2, p);
-    return launch_kernel(grouped_gemv_kernel<6>, dim3((unsigned)grid), dim3(256), smem, lc2, p);
+    const dim3 g3((unsigned)grid), b3(256);
+    if (bits == 4)
+        return per_sm == 1 ? launch_kernel(grouped_gemv_kernel<4, 1>, g3, b3, smem, lc2, p)
+                           : launch_kernel(grouped_gemv_kernel<4, 2>, g3, b3, smem, lc2, p);
+    return per_sm == 1 ? launch_kernel(grouped_gemv_kernel<6, 1>, g3, b3, smem, lc2, p)
+                       : launch_kernel(grouped_gemv_kernel<6, 2>, g3, b3, smem, lc2, p);
 }
 
 }  // namespace qg

@@ -40,11 +40,8 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
 #pragma unroll 2
         for (int b = lane; b < nb; b += 32) {
             const uint4 cw = ldg_stream16(crow + 16 * (size_t)b);
-            Codes32 cc;
-            if constexpr (BITS == 4)
-                cc = unpack_q4(cw);
-            else
-                cc = unpack_q6(cw, ldg_stream8(hrow + 8 * (size_t)b));
+            uint2 hw = make_uint2(0u, 0u);
+            if constexpr (BITS == 6) hw = ldg_stream8(hrow + 8 * (size_t)b);
             const float d = half_bits_to_float(ldg_stream2(srow + b));
             const float m = half_bits_to_float(ldg_stream2(mrow + b));
 #pragma unroll
@@ -53,7 +50,7 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
                     const XqView v = xq_view(smem + c * xstride, nb);
                     const uint4 xl = *reinterpret_cast<const uint4*>(v.lo + 16 * b);
                     const uint4 xh = *reinterpret_cast<const uint4*>(v.hi + 16 * b);
-                    acc[c] += block_combine(block_dot(cc, xl, xh), d, m, v.s[b], v.S[b]);
+                    acc[c] += block_combine(qdot<BITS>(cw, hw, xl, xh), d, m, v.s[b], v.S[b]);
                 }
             }
         }
@@ -114,14 +111,11 @@ __global__ void __launch_bounds__(256) blockdots_kernel(const uint8_t* __restric
         const long long r = t / nb;
         const int b = (int)(t - r * nb);
         const uint4 cw = ldg_stream16(lo + r * (k >> 1) + 16 * b);
-        Codes32 cc;
-        if constexpr (BITS == 4)
-            cc = unpack_q4(cw);
-        else
-            cc = unpack_q6(cw, ldg_stream8(hi + r * (k >> 2) + 8 * b));
+        uint2 hw = make_uint2(0u, 0u);
+        if constexpr (BITS == 6) hw = ldg_stream8(hi + r * (k >> 2) + 8 * b);
         const uint4 xl = *reinterpret_cast<const uint4*>(xq + 32 * b);
         const uint4 xh = *reinterpret_cast<const uint4*>(xq + 32 * b + 16);
-        dots[t] = block_dot(cc, xl, xh);
+        dots[t] = qdot<BITS>(cw, hw, xl, xh);
     }
 }
 

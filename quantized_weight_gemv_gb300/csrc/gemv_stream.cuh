@@ -251,7 +251,10 @@ __global__ void __launch_bounds__(256, BC == 1 ? 2 : 1) gemv_stream_kernel(Strea
         for (int j = 0; j < JPL; ++j) {
             const int fb = lane + 32 * j;
             cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
-            if constexpr (BITS == 6) hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+            if constexpr (BITS == 6)
+                hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+            else
+                hw[j] = make_uint2(0u, 0u);
             dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
             mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
         }
@@ -266,11 +269,7 @@ __global__ void __launch_bounds__(256, BC == 1 ? 2 : 1) gemv_stream_kernel(Strea
 #pragma unroll
         for (int j = 0; j < JPL; ++j) {
             const int rloc = (NB >= SBW) ? 0 : ((lane + 32 * j) >> LOG2NB);
-            Codes32 cc;
-            if constexpr (BITS == 4)
-                cc = unpack_q4(cw[j]);
-            else
-                cc = unpack_q6(cw[j], hw[j]);
+
             const float d = half_bits_to_float(dh[j]);
             const float m = half_bits_to_float(mh[j]);
             const bool valid = rloc < rows_u;
@@ -279,13 +278,13 @@ __global__ void __launch_bounds__(256, BC == 1 ? 2 : 1) gemv_stream_kernel(Strea
                 float r;
                 if constexpr (XREG) {
                     const int xj = NB >= 32 ? (j % NXR) : 0;
-                    r = block_combine(block_dot(cc, xl[c][xj], xh[c][xj]), d, m, xs[c][xj], xS[c][xj]);
+                    r = block_combine(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), d, m, xs[c][xj], xS[c][xj]);
                 } else {
                     const int blk = (part * SBW + lane + 32 * j) & (NB - 1);
                     const XqView v = xq_view(xqbase + c * xstride, NB);
                     const uint4 a = *reinterpret_cast<const uint4*>(v.lo + 16 * blk);
                     const uint4 b = *reinterpret_cast<const uint4*>(v.hi + 16 * blk);
-                    r = block_combine(block_dot(cc, a, b), d, m, v.s[blk], v.S[blk]);
+                    r = block_combine(qdot<BITS>(cw[j], hw[j], a, b), d, m, v.s[blk], v.S[blk]);
                 }
                 pj[c][j] = valid ? r : 0.0f;
             }

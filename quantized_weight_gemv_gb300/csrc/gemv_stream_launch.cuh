@@ -21,11 +21,10 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     constexpr int NB = 1 << L;
     constexpr int W = 8;  // warps per CTA
     const size_t fixed = (size_t)BC * xq_stride(NB);
-    // slots per warp: QG_STREAM_SMEM_KB of shared memory per CTA (default 110 KB, so
-    // that CTAs of two consecutive launches can share an SM under PDL), at least 1
-    const long long budget = (long long)env_int("QG_STREAM_SMEM_KB", 110) * 1024;
-    int D = env_int("QG_STREAM_SLOTS", 0);
-    if (D <= 0) D = (int)((budget - (long long)fixed - 16) / ((long long)W * (SL::BYTES + 8)));
+    // Default: one ring slot per warp and two CTAs per SM (measured on GB300 as the
+    // fastest shape: a slot is refilled as soon as it has been copied to registers).
+    // QG_STREAM_SLOTS (slots per warp) and QG_STREAM_CTAS_PER_SM override it.
+    int D = env_int("QG_STREAM_SLOTS", 1);
     if (D < 1) D = 1;
     if (D > 8) D = 8;
     const size_t cap = (size_t)lc.max_smem_optin - 1024;  // room for static shared memory
@@ -38,7 +37,7 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
     p.stages = D;
     p.err = lc.err;
-    int per_sm = env_int("QG_STREAM_CTAS_PER_SM", 1);
+    int per_sm = env_int("QG_STREAM_CTAS_PER_SM", BC == 1 ? 2 : 1);
     if (per_sm < 1) per_sm = 1;
     int grid = lc.sm_count * per_sm;
     if (EPI == EPI_ARGMAX && grid > VOCAB_MAX_CTAS) grid = VOCAB_MAX_CTAS;

@@ -178,17 +178,51 @@ __device__ __forceinline__ Codes32 unpack_q6(uint4 c, uint2 h) {
     return r;
 }
 
-// sum over the 32 codes of code * xq (codes 0..63 are non-negative in a signed byte)
+// sum over the 32 codes of code * xq (codes 0..63 are non-negative in a signed byte);
+// two independent dp4a chains
 __device__ __forceinline__ int block_dot(const Codes32& c, uint4 xlo, uint4 xhi) {
-    int d = __dp4a((int)c.lo[0], (int)xlo.x, 0);
-    d = __dp4a((int)c.lo[1], (int)xlo.y, d);
-    d = __dp4a((int)c.lo[2], (int)xlo.z, d);
-    d = __dp4a((int)c.lo[3], (int)xlo.w, d);
-    d = __dp4a((int)c.hi[0], (int)xhi.x, d);
-    d = __dp4a((int)c.hi[1], (int)xhi.y, d);
-    d = __dp4a((int)c.hi[2], (int)xhi.z, d);
-    d = __dp4a((int)c.hi[3], (int)xhi.w, d);
+    int a = __dp4a((int)c.lo[0], (int)xlo.x, 0);
+    int b = __dp4a((int)c.hi[0], (int)xhi.x, 0);
+    a = __dp4a((int)c.lo[1], (int)xlo.y, a);
+    b = __dp4a((int)c.hi[1], (int)xhi.y, b);
+    a = __dp4a((int)c.lo[2], (int)xlo.z, a);
+    b = __dp4a((int)c.hi[2], (int)xhi.z, b);
+    a = __dp4a((int)c.lo[3], (int)xlo.w, a);
+    b = __dp4a((int)c.hi[3], (int)xhi.w, b);
+    return a + b;
+}
+
+// dp4a with unsigned bytes in a and signed bytes in b
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
+}
+
+// Q4 block dot straight from the 16 code bytes: the low nibbles are masked out
+// (values 0..15), the high nibbles are masked in place (16 * code, 0..240) and dotted
+// as unsigned bytes, so the second sum is exactly 16x the high-half dot.
+__device__ __forceinline__ int block_dot_q4(uint4 c, uint4 xlo, uint4 xhi) {
+    int a = __dp4a((int)(c.x & 0x0F0F0F0Fu), (int)xlo.x, 0);
+    int b = dp4a_us(c.x & 0xF0F0F0F0u, xhi.x, 0);
+    a = __dp4a((int)(c.y & 0x0F0F0F0Fu), (int)xlo.y, a);
+    b = dp4a_us(c.y & 0xF0F0F0F0u, xhi.y, b);
+    a = __dp4a((int)(c.z & 0x0F0F0F0Fu), (int)xlo.z, a);
+    b = dp4a_us(c.z & 0xF0F0F0F0u, xhi.z, b);
+    a = __dp4a((int)(c.w & 0x0F0F0F0Fu), (int)xlo.w, a);
+    b = dp4a_us(c.w & 0xF0F0F0F0u, xhi.w, b);
+    return a + (b >> 4);
+}
+
+// block dot of either format from its raw words (hw unused for Q4)
+template <int BITS>
+__device__ __forceinline__ int qdot(uint4 cw, uint2 hw, uint4 xlo, uint4 xhi) {
+    if constexpr (BITS == 4) {
+        (void)hw;
+        return block_dot_q4(cw, xlo, xhi);
+    } else {
+        return block_dot(unpack_q6(cw, hw), xlo, xhi);
+    }
 }
 
 // s_b * (scale * D + min * S_b) in fp32

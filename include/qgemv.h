@@ -183,6 +183,26 @@ int qgemv_grouped(int bits, const qg_gemv_desc* descs, int count, void* ws, size
                   void* stream);
 
 /*
+ * qgemv_grouped_noalloc: qgemv_grouped without a caller workspace.  This entry point
+ * has no counterpart in the pages the library follows; it exists for callers that
+ * cannot allocate device memory - code running where the CUDA allocator must not be
+ * called (a host callback, a decode loop that forbids allocation), plug-ins whose
+ * host application owns all device memory, or C callers without an allocator.
+ * The quantised activations go to a fixed QG_NOALLOC_WS_BYTES device array inside
+ * the library, which every GPU that loads the library holds until the process exits.
+ *   Same arguments and results as qgemv_grouped, minus ws/ws_bytes.  A group whose
+ *   activations need more than QG_NOALLOC_WS_BYTES (see qg_grouped_workspace_bytes)
+ *   is rejected with QG_ERR_WORKSPACE and nothing is launched.
+ *   The first call on a device looks up the array's device address (once per device,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls share the array: calls whose work may overlap on the GPU race on it
+ *   and must be ordered by the caller.  It keeps the last call's contents; nothing
+ *   in it needs to start at zero.  The call allocates nothing.
+ */
+#define QG_NOALLOC_WS_BYTES (2u << 20)
+int qgemv_grouped_noalloc(int bits, const qg_gemv_desc* descs, int count, unsigned flags, void* stream);
+
+/*
  * Exposed steps, for exactness checks of the integer parts.
  * qg_quantize_act: per-block int8 quantisation of `batch` rows of x [batch][k]:
  *   xq int8 [batch][k], xs fp32 [batch][k/32] (s_b), xsum int32 [batch][k/32] (sum of xq).

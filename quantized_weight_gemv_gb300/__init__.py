@@ -41,6 +41,7 @@ SIGNATURES = {
     "vocab_softcap_argmax": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _f32p, _f, _f32p, _i32p, _vp, _sz, _u, _vp]),
     "qg_grouped_workspace_bytes": (_sz, [_vp, _i]),
     "qgemv_grouped": (_i, [_i, _vp, _i, _vp, _sz, _u, _vp]),
+    "qgemv_grouped_noalloc": (_i, [_i, _vp, _i, _u, _vp]),
     "qg_quantize_act": (_i, [_f32p, _i, _i, _i8p, _f32p, _i32p, _vp]),
     "qg_blockdots": (_i, [_i, _u8p, _u8p, _i, _i, _i8p, _i32p, _vp]),
 }

@@ -28,6 +28,14 @@ import numpy as np  # noqa: E402
 
 METRIC = "effective weight GB/s & GEMV/s at batch 1 (fraction of ~8 TB/s HBM)"
 
+# DRAM bytes (read + write) per launch of the timed kernel, from one ncu capture of the
+# full decode-layer stream (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None
+# whenever the kernel changes, until it is captured again.
+MEASURED_TRAFFIC = {
+    "grouped": {"kernel": "grouped::grouped_gemv_kernel<4,2>", "bytes_per_launch": 2484.18e6},
+    "percall": None,
+}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -485,7 +493,10 @@ def run_ours(args, ws, rank, local):
     achieved = total_bytes / (ms_step * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks else "fallback",
-                "traffic": None,
+                "traffic": (MEASURED_TRAFFIC[args.launch]["bytes_per_launch"]
+                            if MEASURED_TRAFFIC.get(args.launch) and n_layers == 35 else None),
+                "traffic_unit": "bytes per launch (ncu dram read + write)",
+                "algorithmic_bytes_per_launch": total_bytes if args.launch == "grouped" else total_bytes / n_gemv,
                 "kernel": ("grouped_gemv_kernel (Q4, per-warp bulk-copy rings), one launch per step after the "
                            "activation-quantisation launch it overlaps" if args.launch == "grouped" else
                            "gemv_stream_kernel (Q4, per-warp bulk-copy rings), 245 launches per step") +

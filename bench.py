@@ -60,6 +60,9 @@ CASES = {
     "q4_down_2048x16384": (4, 2048, 16384, 8),
     "q4_q_2048x2048": (4, 2048, 2048, 64),
     "q6_vocab_262144x2048": (6, 262144, 2048, 1),
+    "q4_batched_b4_16384x2048": (4, 16384, 2048, 8),
+    "q4_batched_b8_16384x2048": (4, 16384, 2048, 8),
+    "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
 }
 
 
@@ -76,8 +79,9 @@ def run_case(args):
     w = qg.to_device(datagen.make_quantized(bits, 11, n, k), device)
     rot = [w] + [{kk: (v.clone() if isinstance(v, torch.Tensor) else v) for kk, v in w.items()}
                  for _ in range(copies - 1)]
-    x = torch.from_numpy(datagen.normal_f32(11, 1, k)).to(device)
-    y = torch.empty(n, device=device)
+    batch = int(args.case.split("_batched_b")[1].split("_")[0]) if "_batched_b" in args.case else 1
+    x = torch.from_numpy(datagen.normal_f32(11, 1, batch * k).reshape(batch, k)).to(device)
+    y = torch.empty(batch, n, device=device)
     if bits == 6:
         ws = qg.vocab_workspace(device)
         am = torch.empty(1, dtype=torch.int32, device=device)
@@ -87,17 +91,19 @@ def run_case(args):
     e0.record()
     for i in range(args.reps * copies):
         r = rot[i % copies]
-        if bits == 4:
-            qg.qgemv_q4(r["lo"], r["scale"], r["min"], x, y=y)
+        if batch > 1:
+            qg.qgemv_batched(4, r["lo"], None, r["scale"], r["min"], x, Y=y)
+        elif bits == 4:
+            qg.qgemv_q4(r["lo"], r["scale"], r["min"], x[0], y=y[0])
         else:
-            qg.vocab_softcap_argmax(6, r["lo"], r["hi"], r["scale"], r["min"], x, W.SOFTCAP, logits=y, argmax=am,
-                                    ws=ws)
+            qg.vocab_softcap_argmax(6, r["lo"], r["hi"], r["scale"], r["min"], x[0], W.SOFTCAP, logits=y[0],
+                                    argmax=am, ws=ws)
     e1.record()
     torch.cuda.synchronize()
     calls = args.reps * copies
     nbytes = (W.q4_bytes if bits == 4 else W.q6_bytes)(n, k)
     ms = e0.elapsed_time(e1) / calls
-    print(json.dumps({"case": args.case, "calls": calls, "us_per_call_eager": ms * 1e3,
+    print(json.dumps({"case": args.case, "batch": batch, "calls": calls, "us_per_call_eager": ms * 1e3,
                       "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
 
 

@@ -104,12 +104,16 @@ static int gemv_common(int bits, const uint8_t* lo, const uint8_t* hi, const uin
     LaunchCtx lc;
     rc = resolve(stream, flags, lc);
     if (rc != QG_OK) return rc;
+    PlainParams pp = {lo, hi, scale, min, n, k, batch, x, y, 0.0f, nullptr, nullptr};
+    if (!(flags & QG_FLAG_PLAIN) && mma_supported(bits, k, batch)) {
+        rc = launch_mma(pp, lc);
+        if (rc != QG_ERR_UNSUPPORTED) return rc;
+    }
     if (!(flags & QG_FLAG_PLAIN) && stream_supported(bits, n, k, batch, EPI_STORE)) {
         StreamParams sp = {lo, hi, scale, min, n, k, batch, 0, 0, x, y, 0.0f, nullptr, nullptr, nullptr};
         rc = launch_stream(sp, bits, EPI_STORE, lc);
         if (rc != QG_ERR_UNSUPPORTED) return rc;
     }
-    PlainParams pp = {lo, hi, scale, min, n, k, batch, x, y, 0.0f, nullptr, nullptr};
     return launch_plain(pp, bits, EPI_STORE, lc);
 }
 

@@ -21,8 +21,7 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
     pdl_wait();  // x, y and the workspace may belong to the preceding kernel
     if (threadIdx.x == 0) pdl_launch_dependents();
 
-    for (int c = 0; c < p.batch; ++c)
-        quantize_x_coop<256>(p.x + (size_t)c * p.k, p.k, xq_view(smem + c * xstride, nb), threadIdx.x);
+    quantize_x_cols<256>(p.x, p.k, p.batch, smem, xstride, threadIdx.x);
     __syncthreads();
 
     float bv = __int_as_float(0x7fc00000);

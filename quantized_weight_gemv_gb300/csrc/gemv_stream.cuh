@@ -148,7 +148,7 @@ __device__ __forceinline__ void emit_row(const StreamParams& p, long long row, c
 }
 
 template <int BITS, int BC, int EPI, int LOG2NB>
-__global__ void __launch_bounds__(256, BC == 1 ? 2 : 1) gemv_stream_kernel(StreamParams p) {
+__global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(StreamParams p) {
     using SL = Slot<BITS>;
     constexpr int NB = 1 << LOG2NB;
     constexpr int R = NB >= SBW ? 1 : SBW / NB;       // rows per stage
@@ -203,8 +203,7 @@ __global__ void __launch_bounds__(256, BC == 1 ? 2 : 1) gemv_stream_kernel(Strea
 
     // ---- activation prologue (after the preceding kernel, which may have written x)
     pdl_wait();
-    for (int c = 0; c < p.batch; ++c)
-        quantize_x_coop<256>(p.x + (size_t)c * p.k, p.k, xq_view(xqbase + c * xstride, NB), threadIdx.x);
+    quantize_x_cols<256>(p.x, p.k, p.batch, xqbase, xstride, threadIdx.x);
     __syncthreads();
 
     uint4 xl[BC][NXR], xh[BC][NXR];

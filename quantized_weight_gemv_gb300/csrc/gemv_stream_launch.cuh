@@ -37,7 +37,7 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
     p.stages = D;
     p.err = lc.err;
-    int per_sm = env_int("QG_STREAM_CTAS_PER_SM", BC == 1 ? 2 : 1);
+    int per_sm = env_int("QG_STREAM_CTAS_PER_SM", BC <= 2 ? 2 : 1);
     if (per_sm < 1) per_sm = 1;
     int grid = lc.sm_count * per_sm;
     if (EPI == EPI_ARGMAX && grid > VOCAB_MAX_CTAS) grid = VOCAB_MAX_CTAS;

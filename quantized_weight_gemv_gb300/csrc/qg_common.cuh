@@ -92,27 +92,31 @@ __device__ __forceinline__ XqView xq_view(unsigned char* base, int nb) {
 }
 __host__ __device__ constexpr int xq_bytes(int nb) { return 40 * nb; }
 
-// Cooperative quantisation of x[k] into an XqView by NT threads (t = 0..NT-1, whole
-// warps).  Thread t takes float4 number i*NT + t: eight consecutive lanes hold one
-// block of 32, so a block's max and sum need three shuffles.  All loads of a round
-// are issued before any use, so the prologue costs about one L2 round trip per
-// CHUNK float4 per thread instead of one per block.
+// Cooperative quantisation of `batch` activation columns x[c][k] into per-column
+// XqViews (column c at base + c * stride) by NT threads (t = 0..NT-1, whole warps).
+// The float4s of all columns form one index space; thread t takes number i*NT + t,
+// so eight consecutive lanes hold one block of 32 of one column and a block's max
+// and sum need three shuffles.  All CHUNK loads of a round are issued before any is
+// used, so the prologue costs about one L2 round trip per CHUNK*NT float4s.
 template <int NT>
-__device__ __forceinline__ void quantize_x_coop(const float* __restrict__ x, int k, XqView v, int t) {
+__device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int k, int batch, unsigned char* base,
+                                                int stride, int t) {
     constexpr int CHUNK = 8;
+    const int nb = k >> 5;
     const int nf4 = k >> 2;  // a multiple of 8
+    const int total = batch * nf4;
     const int m = t & 7;     // float4 index within the block
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    for (int base = 0; base < nf4; base += NT * CHUNK) {
+    for (int r0 = 0; r0 < total; r0 += NT * CHUNK) {
         float4 r[CHUNK];
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
-            const int idx = base + i * NT + t;
-            r[i] = idx < nf4 ? __ldg(x4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int idx = r0 + i * NT + t;
+            r[i] = idx < total ? __ldg(x4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
-            const int idx = base + i * NT + t;
+            const int idx = r0 + i * NT + t;
             float a = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
@@ -129,8 +133,10 @@ __device__ __forceinline__ void quantize_x_coop(const float* __restrict__ x, int
             S += __shfl_xor_sync(0xffffffffu, S, 1);
             S += __shfl_xor_sync(0xffffffffu, S, 2);
             S += __shfl_xor_sync(0xffffffffu, S, 4);
-            if (idx < nf4) {
-                const int b = idx >> 3;
+            if (idx < total) {
+                const int c = idx / nf4;
+                const int b = (idx - c * nf4) >> 3;
+                const XqView v = xq_view(base + (size_t)c * stride, nb);
                 const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
                                         ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
                 int8_t* dst = m < 4 ? v.lo + 16 * b + 4 * m : v.hi + 16 * b + 4 * (m - 4);

@@ -105,9 +105,18 @@ int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const 
  *   bits : 4 (hi must be NULL) or 6
  *   1 <= batch <= QG_MAX_BATCH;  batch * k <= 131072
  *   X : device fp32 [batch][k];  Y : device fp32 [batch][n] (written)
+ * For batch >= 8 with 4-bit weights and k in {512, 1024, 2048, 4096} the integer
+ * block dots run on tensor cores (mma.sync, f16 operands, exact).  That path quantises
+ * the activations once into `ws` (at least qg_batched_workspace_bytes(bits, k, batch)
+ * bytes of device memory, 16-byte aligned, no initial content; 0 bytes are needed for
+ * the other shapes) and chains the GEMV launch to it by programmatic dependent
+ * launch; with ws == NULL every CTA quantises the activations itself (slower).
+ * Calls that share a workspace must not overlap on the GPU.
  */
+size_t qg_batched_workspace_bytes(int bits, int k, int batch);
 int qgemv_batched(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n,
-                  int k, int batch, const float* X, float* Y, unsigned flags, void* stream);
+                  int k, int batch, const float* X, float* Y, void* ws, size_t ws_bytes, unsigned flags,
+                  void* stream);
 
 /*
  * cq_fwht_matvec: selected-row codebook matvec in the Hadamard domain

@@ -35,7 +35,8 @@ SIGNATURES = {
     "qg_device_error": (_i, [ctypes.POINTER(ctypes.c_uint32)]),
     "qgemv_q4": (_i, [_u8p, _u16p, _u16p, _i, _i, _f32p, _f32p, _u, _vp]),
     "qgemv_q6": (_i, [_u8p, _u8p, _u16p, _u16p, _i, _i, _f32p, _f32p, _u, _vp]),
-    "qgemv_batched": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _i, _f32p, _f32p, _u, _vp]),
+    "qg_batched_workspace_bytes": (_sz, [_i, _i, _i]),
+    "qgemv_batched": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _i, _f32p, _f32p, _vp, _sz, _u, _vp]),
     "cq_fwht_matvec": (_i, [_u8p, _u16p, _u16p, _i, _i, _i, _i, _i, _f32p, _f32p, _u, _vp]),
     "qg_vocab_workspace_bytes": (_sz, []),
     "vocab_softcap_argmax": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _f32p, _f, _f32p, _i32p, _vp, _sz, _u, _vp]),
@@ -145,8 +146,15 @@ def qgemv_q6(lo, hi, scale, min, x, y=None, flags: int = 0):
     return y
 
 
-def qgemv_batched(bits, lo, hi, scale, min, X, Y=None, flags: int = 0):
-    """Y[batch][n] for activation columns X[batch][k] sharing one pass over the weights."""
+def batched_workspace(bits, k, batch, device):
+    """A workspace for :func:`qgemv_batched` (None when the shape needs none)."""
+    nbytes = int(lib().qg_batched_workspace_bytes(bits, k, batch))
+    return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes else None
+
+
+def qgemv_batched(bits, lo, hi, scale, min, X, Y=None, flags: int = 0, ws="auto"):
+    """Y[batch][n] for activation columns X[batch][k] sharing one pass over the weights.
+    ``ws``: a workspace tensor, None (no workspace: slower for batch >= 8), or "auto"."""
     _need(lo, "lo", _U8)
     dev = lo.device
     if bits == 6:
@@ -159,9 +167,14 @@ def qgemv_batched(bits, lo, hi, scale, min, X, Y=None, flags: int = 0):
     if Y is None:
         Y = torch.empty(batch, n, dtype=torch.float32, device=dev)
     _need(Y, "Y", _F32, dev)
+    if isinstance(ws, str):
+        ws = batched_workspace(bits, k, batch, dev)
+    if ws is not None:
+        _need(ws, "ws", None, dev)
     with torch.cuda.device(dev):
         _check(lib().qgemv_batched(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min), n, k,
-                                   batch, _ptr(X), _ptr(Y), flags, _stream(dev)), "qgemv_batched")
+                                   batch, _ptr(X), _ptr(Y), _ptr(ws), 0 if ws is None else ws.numel(), flags,
+                                   _stream(dev)), "qgemv_batched")
     return Y
 
 

@@ -94,19 +94,25 @@ static int check_weights(int bits, const uint8_t* lo, const uint8_t* hi, const u
 }
 
 static int gemv_common(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
-                       int n, int k, int batch, const float* x, float* y, unsigned flags, void* stream) {
+                       int n, int k, int batch, const float* x, float* y, void* ws, size_t ws_bytes, unsigned flags,
+                       void* stream) {
     int rc = check_weights(bits, lo, hi, scale, min, n, k);
     if (rc != QG_OK) return rc;
     if (batch < 1 || batch > QG_MAX_BATCH || (long long)batch * k > 131072) return QG_ERR_INVALID_ARG;
     if (n == 0) return QG_OK;
     if (!x || !y) return QG_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y)) return QG_ERR_ALIGNMENT;
+    const bool use_mma = !(flags & QG_FLAG_PLAIN) && mma_supported(bits, k, batch);
+    if (ws) {
+        if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
+        if (use_mma && ws_bytes < mma_workspace_bytes(k, batch)) return QG_ERR_WORKSPACE;
+    }
     LaunchCtx lc;
     rc = resolve(stream, flags, lc);
     if (rc != QG_OK) return rc;
     PlainParams pp = {lo, hi, scale, min, n, k, batch, x, y, 0.0f, nullptr, nullptr};
-    if (!(flags & QG_FLAG_PLAIN) && mma_supported(bits, k, batch)) {
-        rc = launch_mma(pp, lc);
+    if (use_mma) {
+        rc = launch_mma(pp, reinterpret_cast<unsigned char*>(ws), lc);
         if (rc != QG_ERR_UNSUPPORTED) return rc;
     }
     if (!(flags & QG_FLAG_PLAIN) && stream_supported(bits, n, k, batch, EPI_STORE)) {
@@ -155,18 +161,24 @@ int qg_device_error(uint32_t* code) {
 
 int qgemv_q4(const uint8_t* codes, const uint16_t* scale, const uint16_t* min, int n, int k, const float* x,
              float* y, unsigned flags, void* stream) {
-    return gemv_common(4, codes, nullptr, scale, min, n, k, 1, x, y, flags, stream);
+    return gemv_common(4, codes, nullptr, scale, min, n, k, 1, x, y, nullptr, 0, flags, stream);
 }
 
 int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n, int k,
              const float* x, float* y, unsigned flags, void* stream) {
     if (!hi && n > 0) return QG_ERR_INVALID_ARG;
-    return gemv_common(6, lo, hi, scale, min, n, k, 1, x, y, flags, stream);
+    return gemv_common(6, lo, hi, scale, min, n, k, 1, x, y, nullptr, 0, flags, stream);
+}
+
+size_t qg_batched_workspace_bytes(int bits, int k, int batch) {
+    if (k <= 0 || (k & 31) != 0 || k > QG_MAX_K || batch < 1 || batch > QG_MAX_BATCH) return 0;
+    return mma_supported(bits, k, batch) ? mma_workspace_bytes(k, batch) : 0;
 }
 
 int qgemv_batched(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n,
-                  int k, int batch, const float* X, float* Y, unsigned flags, void* stream) {
-    return gemv_common(bits, lo, hi, scale, min, n, k, batch, X, Y, flags, stream);
+                  int k, int batch, const float* X, float* Y, void* ws, size_t ws_bytes, unsigned flags,
+                  void* stream) {
+    return gemv_common(bits, lo, hi, scale, min, n, k, batch, X, Y, ws, ws_bytes, flags, stream);
 }
 
 int cq_fwht_matvec(const uint8_t* idx, const uint16_t* codebook, const uint16_t* row_scale, int n, int k, int group,

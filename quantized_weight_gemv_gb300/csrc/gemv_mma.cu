@@ -40,6 +40,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+// d = a * b + c
+__device__ __forceinline__ void mma_16816_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                              const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
 __device__ __forceinline__ uint32_t hsub1024(uint32_t v) {
     const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), __half2half2(__ushort_as_half(0x6400)));
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -59,8 +69,11 @@ __device__ __forceinline__ void a_frags(uint32_t w0, uint32_t w1, uint32_t (&lo)
     hi[3] = hsub1024((q1 & 0x00F000F0u) | 0x64006400u);
 }
 
-__device__ __forceinline__ uint32_t pack_h2(int a, int b) {
-    const __half2 h = __halves2half2(__int2half_rn(a), __int2half_rn(b));
+// two int8 activations as f16, optionally divided by 16 (exact: |q|/16 has at most
+// 7 significant bits)
+__device__ __forceinline__ uint32_t pack_h2(int a, int b, bool div16) {
+    const float f = div16 ? 0.0625f : 1.0f;
+    const __half2 h = __halves2half2(__float2half_rn((float)a * f), __float2half_rn((float)b * f));
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
@@ -74,23 +87,28 @@ struct Smem {
     __host__ __device__ static size_t bytes(int nb) { return part_off(nb) + (size_t)NW * 16 * 8 * NT * 4; }
 };
 
-// Quantise the B activation columns straight into B fragments.  float4 number idx of
-// column c (elements 4m..4m+3 of block b, m = idx & 7) becomes the fragment of lane
-// 4*(c%8) + (m%4), k half m/4, tile c/8.
+// Quantise the B activation columns straight into B fragments (image layout as
+// Smem<NT> without the partial sums).  float4 number idx of column c (elements
+// 4m..4m+3 of block b, m = idx & 7) becomes the fragment of lane 4*(c%8) + (m%4),
+// k half m/4, tile c/8; the high half (m >= 4) holds x/16, so that its product with
+// the 16x high-nibble codes accumulates onto the low half exactly.  Items
+// [item0, item0 + nthreads * rounds) of the 8*NT*k/4 float4s are done by threads
+// t = 0..nthreads-1 (whole warps).
 template <int NT>
-__device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, int k, int batch, unsigned char* sm) {
+__device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, int k, int batch, unsigned char* img,
+                                                  int t, int nthreads, int item0, int item_end) {
     const int nb = k >> 5;
-    uint2* frag = reinterpret_cast<uint2*>(sm);
-    float* sv = reinterpret_cast<float*>(sm + Smem<NT>::sv_off(nb));
-    float* Sv = reinterpret_cast<float*>(sm + Smem<NT>::Sv_off(nb));
+    uint2* frag = reinterpret_cast<uint2*>(img);
+    float* sv = reinterpret_cast<float*>(img + Smem<NT>::sv_off(nb));
+    float* Sv = reinterpret_cast<float*>(img + Smem<NT>::Sv_off(nb));
     const int nf4 = k >> 2;
-    const int total = 8 * NT * nf4;  // columns beyond the batch quantise zeros
+    const int total = min(8 * NT * nf4, item_end);  // columns beyond the batch quantise zeros
     constexpr int CHUNK = 8;
-    for (int r0 = 0; r0 < total; r0 += NW * 32 * CHUNK) {
+    for (int r0 = item0; r0 < total; r0 += nthreads * CHUNK) {
         float4 rv[CHUNK];
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
-            const int idx_all = r0 + i * NW * 32 + threadIdx.x;
+            const int idx_all = r0 + i * nthreads + t;
             const int c = idx_all / nf4;
             rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (idx_all < total && c < batch)
@@ -98,7 +116,7 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
         }
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
-            const int idx_all = r0 + i * NW * 32 + threadIdx.x;
+            const int idx_all = r0 + i * nthreads + t;
             const int c = idx_all / nf4;
             const int idx = idx_all - c * nf4;
             const float4 r = rv[i];
@@ -121,8 +139,9 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
             if (idx_all < total) {
                 const int b = idx >> 3, m = idx & 7;
                 const int lane = 4 * (c & 7) + (m & 3);
-                frag[(((size_t)b * 2 + (m >> 2)) * NT + (c >> 3)) * 32 + lane] =
-                    make_uint2(pack_h2(q0, q1), pack_h2(q2, q3));
+                const bool hi = m >= 4;
+                frag[((b * 2 + (m >> 2)) * NT + (c >> 3)) * 32 + lane] =
+                    make_uint2(pack_h2(q0, q1, hi), pack_h2(q2, q3, hi));
                 if (m == 0) {
                     sv[b * 8 * NT + c] = s;
                     Sv[b * 8 * NT + c] = (float)S;
@@ -132,9 +151,55 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
     }
 }
 
+// The activation image, once per call, into the workspace (kernel 1 of 2).
 template <int NT>
-__global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p) {
+__global__ void __launch_bounds__(256) mma_prep_kernel(const float* __restrict__ X, int k, int batch,
+                                                       unsigned char* __restrict__ img) {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    const int per_cta = 256 * 8;
+    const int item0 = blockIdx.x * per_cta;
+    quantize_to_frags<NT>(X, k, batch, img, threadIdx.x, 256, item0, item0 + per_cta);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Weights of four consecutive blocks for a thread's two rows: code words and the
+// scales/mins as binary16 pairs (blocks 2i, 2i+1 of the step in word i).
+struct StepRegs {
+    uint32_t w0[4], w1[4];
+    uint32_t dA[2], dB[2], mA[2], mB[2];
+};
+
+__device__ __forceinline__ void load_step(StepRegs& r, const uint8_t* ca, const uint8_t* cb, const uint16_t* da,
+                                          const uint16_t* db, const uint16_t* ma, const uint16_t* mb, int b0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        r.w0[j] = __ldg(reinterpret_cast<const unsigned int*>(ca + 16 * (b0 + j)));
+        r.w1[j] = __ldg(reinterpret_cast<const unsigned int*>(cb + 16 * (b0 + j)));
+    }
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(da + b0));
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(db + b0));
+    const uint2 c = __ldg(reinterpret_cast<const uint2*>(ma + b0));
+    const uint2 e = __ldg(reinterpret_cast<const uint2*>(mb + b0));
+    r.dA[0] = a.x; r.dA[1] = a.y;
+    r.dB[0] = b.x; r.dB[1] = b.y;
+    r.mA[0] = c.x; r.mA[1] = c.y;
+    r.mB[0] = e.x; r.mB[1] = e.y;
+}
+
+// binary16 j (0..3) of a pair array, as float
+__device__ __forceinline__ float half_of(const uint32_t (&w)[2], int j) {
+    return half_bits_to_float((unsigned short)(w[j >> 1] >> (16 * (j & 1))));
+}
+
+// The GEMV (kernel 2 of 2, or alone without a workspace).  With PREP the activation
+// image comes from the workspace in one bulk copy; without, every CTA quantises.
+template <int NT, bool PREP>
+__global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p, const unsigned char* img,
+                                                                 unsigned int* err) {
     extern __shared__ __align__(16) unsigned char sm[];
+    __shared__ __align__(8) uint64_t img_bar;
     const int nb = p.k >> 5;
     const int QC = nb / KC;     // k chunks per row group (1, 2, 4 or 8)
     const int RG = NW / QC;     // row groups per CTA pass
@@ -144,7 +209,40 @@ __global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p) 
 
     pdl_wait();
     if (threadIdx.x == 0) pdl_launch_dependents();
-    quantize_to_frags<NT>(p.x, p.k, p.batch, sm);
+    if constexpr (PREP) {
+        const uint32_t bytes = (uint32_t)Smem<NT>::part_off(nb);
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&img_bar)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&img_bar)),
+                         "r"(bytes)
+                         : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(sm)),
+                "l"(img), "r"(bytes), "r"(smem_u32(&img_bar))
+                : "memory");
+        }
+        __syncthreads();  // the barrier is initialised before anyone polls it
+        uint32_t ok = 0;
+        const unsigned long long t0 = globaltimer_ns();
+        for (;;) {
+            asm volatile(
+                "{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(ok)
+                : "r"(smem_u32(&img_bar))
+                : "memory");
+            if (ok || globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+        }
+        // give up together if the copy never landed (bounded wait), leaving the error word set
+        if (__syncthreads_or(ok == 0)) {
+            if (threadIdx.x == 0) atomicOr(err, ERR_WAIT_FULL);
+            return;
+        }
+    } else {
+        quantize_to_frags<NT>(p.x, p.k, p.batch, sm, threadIdx.x, NW * 32, 0, 1 << 30);
+    }
     __syncthreads();
 
     const uint2* frag = reinterpret_cast<const uint2*>(sm);
@@ -167,41 +265,34 @@ __global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p) 
             const uint16_t* db = p.scale + (size_t)rb * nb;
             const uint16_t* ma = p.min + (size_t)ra * nb;
             const uint16_t* mb = p.min + (size_t)rb * nb;
-#pragma unroll 1
-            for (int half = 0; half < KC; half += 8) {
-                const int b0 = my_q * KC + half;
-                uint32_t w0[8], w1[8];
-                unsigned short dA[8], dB[8], mA[8], mB[8];
+            // four steps of four blocks; the loads of step i+1 are in flight while step i computes
+            StepRegs buf[2];
+            load_step(buf[0], ca, cb, da, db, ma, mb, my_q * KC);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    w0[j] = __ldg(reinterpret_cast<const unsigned int*>(ca + 16 * (b0 + j)));
-                    w1[j] = __ldg(reinterpret_cast<const unsigned int*>(cb + 16 * (b0 + j)));
-                    dA[j] = __ldg(da + b0 + j);
-                    dB[j] = __ldg(db + b0 + j);
-                    mA[j] = __ldg(ma + b0 + j);
-                    mB[j] = __ldg(mb + b0 + j);
-                }
+            for (int step = 0; step < KC / 4; ++step) {
+                if (step + 1 < KC / 4) load_step(buf[(step + 1) & 1], ca, cb, da, db, ma, mb, my_q * KC + 4 * (step + 1));
+                const StepRegs& cur = buf[step & 1];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int b = b0 + j;
+                for (int j = 0; j < 4; ++j) {
+                    const int b = my_q * KC + 4 * step + j;
                     uint32_t alo[4], ahi[4];
-                    a_frags(w0[j], w1[j], alo, ahi);
-                    const float d0 = half_bits_to_float(dA[j]), d1 = half_bits_to_float(dB[j]);
-                    const float m0 = half_bits_to_float(mA[j]), m1 = half_bits_to_float(mB[j]);
+                    a_frags(cur.w0[j], cur.w1[j], alo, ahi);
+                    const float d0 = half_of(cur.dA, j), d1 = half_of(cur.dB, j);
+                    const float m0 = half_of(cur.mA, j), m1 = half_of(cur.mB, j);
 #pragma unroll
                     for (int tt = 0; tt < NT; ++tt) {
-                        const uint2 bl = frag[(((size_t)b * 2 + 0) * NT + tt) * 32 + lane];
-                        const uint2 bh = frag[(((size_t)b * 2 + 1) * NT + tt) * 32 + lane];
-                        float dl[4], dh[4];
+                        const uint2 bl = frag[((b * 2 + 0) * NT + tt) * 32 + lane];
+                        const uint2 bh = frag[((b * 2 + 1) * NT + tt) * 32 + lane];
+                        float dl[4], D[4];
                         mma_16816(dl, alo, bl.x, bl.y);
-                        mma_16816(dh, ahi, bh.x, bh.y);
+                        mma_16816_acc(D, ahi, bh.x, bh.y, dl);  // exact integer block dots
                         const float2 s2 = *reinterpret_cast<const float2*>(sv + b * 8 * NT + tt * 8 + 2 * t);
                         const float2 S2 = *reinterpret_cast<const float2*>(Sv + b * 8 * NT + tt * 8 + 2 * t);
                         // (row g, col 2t), (row g, col 2t+1), (row g+8, col 2t), (row g+8, col 2t+1)
-                        acc[tt][0] += s2.x * fmaf(d0, fmaf(dh[0], 0.0625f, dl[0]), m0 * S2.x);
-                        acc[tt][1] += s2.y * fmaf(d0, fmaf(dh[1], 0.0625f, dl[1]), m0 * S2.y);
-                        acc[tt][2] += s2.x * fmaf(d1, fmaf(dh[2], 0.0625f, dl[2]), m1 * S2.x);
-                        acc[tt][3] += s2.y * fmaf(d1, fmaf(dh[3], 0.0625f, dl[3]), m1 * S2.y);
+                        acc[tt][0] = fmaf(s2.x, fmaf(d0, D[0], m0 * S2.x), acc[tt][0]);
+                        acc[tt][1] = fmaf(s2.y, fmaf(d0, D[1], m0 * S2.y), acc[tt][1]);
+                        acc[tt][2] = fmaf(s2.x, fmaf(d1, D[2], m1 * S2.x), acc[tt][2]);
+                        acc[tt][3] = fmaf(s2.y, fmaf(d1, D[3], m1 * S2.y), acc[tt][3]);
                     }
                 }
             }
@@ -239,19 +330,39 @@ bool mma_supported(int bits, int k, int batch) {
     return bits == 4 && batch >= 8 && batch <= 16 && (nb == 16 || nb == 32 || nb == 64 || nb == 128);
 }
 
-int launch_mma(const PlainParams& p, const LaunchCtx& lc) {
+size_t mma_workspace_bytes(int k, int batch) {
+    const int nb = k >> 5;
+    return batch <= 8 ? mma::Smem<1>::part_off(nb) : mma::Smem<2>::part_off(nb);
+}
+
+template <int NT>
+static int launch_mma_t(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc) {
     const int nb = p.k >> 5;
     const int QC = nb / mma::KC, RG = mma::NW / QC;
     const int n_groups = (p.n + 15) >> 4;
-    const int NT = p.batch <= 8 ? 1 : 2;
-    const size_t smem = NT == 1 ? mma::Smem<1>::bytes(nb) : mma::Smem<2>::bytes(nb);
-    const void* kern = NT == 1 ? (const void*)mma::mma_batched_kernel<1> : (const void*)mma::mma_batched_kernel<2>;
-    if (int rc = ensure_smem_attr(kern, smem, lc)) return rc;
+    const size_t smem = mma::Smem<NT>::bytes(nb);
     int grid = (n_groups + RG - 1) / RG;
     if (grid > lc.sm_count * 2) grid = lc.sm_count * 2;
     if (grid < 1) grid = 1;
-    if (NT == 1) return launch_kernel(mma::mma_batched_kernel<1>, dim3(grid), dim3(mma::NW * 32), smem, lc, p);
-    return launch_kernel(mma::mma_batched_kernel<2>, dim3(grid), dim3(mma::NW * 32), smem, lc, p);
+    if (!ws) {
+        auto kern = mma::mma_batched_kernel<NT, false>;
+        if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
+        return launch_kernel(kern, dim3(grid), dim3(mma::NW * 32), smem, lc, p, (const unsigned char*)nullptr, lc.err);
+    }
+    // 1. the activation image, once; 2. the GEMV, chained by programmatic dependent launch
+    const int items = 8 * NT * (p.k >> 2);
+    const int pgrid = (items + 256 * 8 - 1) / (256 * 8);
+    int rc = launch_kernel(mma::mma_prep_kernel<NT>, dim3(pgrid), dim3(256), 0, lc, p.x, p.k, p.batch, ws);
+    if (rc != QG_OK) return rc;
+    auto kern = mma::mma_batched_kernel<NT, true>;
+    if (int e = ensure_smem_attr((const void*)kern, smem, lc)) return e;
+    LaunchCtx lc2 = lc;
+    lc2.flags |= QG_FLAG_PDL;
+    return launch_kernel(kern, dim3(grid), dim3(mma::NW * 32), smem, lc2, p, (const unsigned char*)ws, lc.err);
+}
+
+int launch_mma(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc) {
+    return p.batch <= 8 ? launch_mma_t<1>(p, ws, lc) : launch_mma_t<2>(p, ws, lc);
 }
 
 }  // namespace qg

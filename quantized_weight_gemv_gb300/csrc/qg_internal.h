@@ -93,7 +93,9 @@ bool stream_supported(int bits, int n, int k, int batch, int epi);
 int launch_cq(const CqParams& p, const LaunchCtx& lc);
 // tensor-core small-batch MMVQ (Q4, batch 8..16)
 bool mma_supported(int bits, int k, int batch);
-int launch_mma(const PlainParams& p, const LaunchCtx& lc);
+size_t mma_workspace_bytes(int k, int batch);
+// ws: the activation image (mma_workspace_bytes), or null to quantise in every CTA
+int launch_mma(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc);
 size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count);
 int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc);
 int launch_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, const LaunchCtx& lc);

@@ -74,11 +74,15 @@ def test_q6_and_batched_validation(lib):
     assert lib.qgemv_q6(A16, None, A16, A16, 4, 64, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
     assert lib.qgemv_q6(A16, MIS, A16, A16, 4, 64, A16, A16, 0, None) == qg.QG_ERR_ALIGNMENT
     b = lib.qgemv_batched
-    assert b(5, A16, None, A16, A16, 4, 64, 1, A16, A16, 0, None) == qg.QG_ERR_UNSUPPORTED
-    assert b(4, A16, A16, A16, A16, 4, 64, 1, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG  # hi given for Q4
-    assert b(4, A16, None, A16, A16, 4, 64, 0, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
-    assert b(4, A16, None, A16, A16, 4, 64, 17, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
-    assert b(4, A16, None, A16, A16, 4, 16384, 16, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG  # batch*k too big
+    assert b(5, A16, None, A16, A16, 4, 64, 1, A16, A16, None, 0, 0, None) == qg.QG_ERR_UNSUPPORTED
+    assert b(4, A16, A16, A16, A16, 4, 64, 1, A16, A16, None, 0, 0, None) == qg.QG_ERR_INVALID_ARG  # hi for Q4
+    assert b(4, A16, None, A16, A16, 4, 64, 0, A16, A16, None, 0, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert b(4, A16, None, A16, A16, 4, 64, 17, A16, A16, None, 0, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert b(4, A16, None, A16, A16, 4, 16384, 16, A16, A16, None, 0, 0, None) == qg.QG_ERR_INVALID_ARG
+    need = lib.qg_batched_workspace_bytes(4, 2048, 16)
+    assert need > 0 and lib.qg_batched_workspace_bytes(4, 2048, 4) == 0 and lib.qg_batched_workspace_bytes(6, 2048, 16) == 0
+    assert b(4, A16, None, A16, A16, 4, 2048, 16, A16, A16, A16, need - 1, 0, None) == qg.QG_ERR_WORKSPACE
+    assert b(4, A16, None, A16, A16, 4, 2048, 16, A16, A16, MIS, need, 0, None) == qg.QG_ERR_ALIGNMENT
 
 
 def test_cq_validation(lib):

@@ -343,3 +343,19 @@ def test_grouped_many_descriptors():
     qg.qgemv_grouped(4, mats, xs, ys)
     for y, r in zip(ys, ref):
         assert_close(y.cpu().numpy().astype(np.float64), r)
+
+
+@pytest.mark.parametrize("batch", [8, 12, 16])
+@pytest.mark.parametrize("k", [512, 1024, 2048, 4096])
+def test_batched_tensor_core_with_and_without_workspace(batch, k):
+    """The tensor-core path quantises once into a workspace, or per CTA without one; both match the oracle."""
+    n = 777
+    w = datagen.make_quantized(4, 900 + k + batch, n, k)
+    X = datagen.normal_f32(900 + k + batch, 1, batch * k).reshape(batch, k)
+    wd = dev_w(w)
+    Xt = torch.from_numpy(X).to(DEV)
+    refs = [oracle.gemv(w, X[b]) for b in range(batch)]
+    for ws in ("auto", None):
+        Y = qg.qgemv_batched(4, wd["lo"], None, wd["scale"], wd["min"], Xt, ws=ws).cpu().numpy()
+        for b in range(batch):
+            assert_close(Y[b], refs[b])

@@ -19,9 +19,12 @@
 //    0x6400 | c read as half are 1024 + c, minus 1024 exactly.
 //  * the B fragments (activations) are written in the same permuted order straight
 //    from the quantisation: each float4 of x quantises to exactly one 8-byte fragment.
-//  * warps of a CTA split a group of 16-row blocks by k chunks of 512; partial sums
-//    meet in shared memory.  Code words, scales and mins are loaded from global
-//    memory straight into registers, eight blocks ahead.
+//  * the activation image is made once per call into a workspace (prep kernel) and
+//    pulled into shared memory with one bulk copy; 16 warps per CTA share it.
+//  * each warp owns tiles of 16 rows x 8 blocks and streams them through a private
+//    two-stage cp.async ring (rows padded to 144 bytes so that the fragment reads
+//    are bank-conflict free); the warps of a row group split k and their partial
+//    sums meet in shared memory.
 #include <cuda_fp16.h>
 
 #include "qg_internal.h"
@@ -29,8 +32,9 @@
 namespace qg {
 namespace mma {
 
-constexpr int KC = 16;  // blocks per k chunk (512 elements)
-constexpr int NW = 8;   // warps per CTA
+constexpr int KC = 8;     // blocks per tile (256 elements of k)
+constexpr int NW = 16;    // warps per CTA
+constexpr int DEPTH = 2;  // tiles in flight per warp
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -77,14 +81,23 @@ __device__ __forceinline__ uint32_t pack_h2(int a, int b, bool div16) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Shared layout: frag[nb][2][NT][32] uint2 | sv[nb][8*NT] f32 | Sv[nb][8*NT] f32 | part[NW][16][8*NT] f32
+// A weight tile in shared memory: codes [16 rows][144 B] (8 blocks + 16 B of padding),
+// scale [16][8] and min [16][8] binary16.
+constexpr int TILE_ROW = 144;
+constexpr int TILE_CODES = 16 * TILE_ROW;
+constexpr int TILE_BYTES = TILE_CODES + 2 * 16 * 16;
+
+// Shared layout: frag[nb][2][NT][32] uint2 | sv[nb][8*NT] f32 | Sv[nb][8*NT] f32 (the
+// activation image, also the workspace layout) | part[NW][16][8*NT] f32 |
+// tiles[NW][DEPTH]
 template <int NT>
 struct Smem {
     __host__ __device__ static size_t frag_bytes(int nb) { return (size_t)nb * 2 * NT * 32 * 8; }
     __host__ __device__ static size_t sv_off(int nb) { return frag_bytes(nb); }
     __host__ __device__ static size_t Sv_off(int nb) { return sv_off(nb) + (size_t)nb * 8 * NT * 4; }
     __host__ __device__ static size_t part_off(int nb) { return Sv_off(nb) + (size_t)nb * 8 * NT * 4; }
-    __host__ __device__ static size_t bytes(int nb) { return part_off(nb) + (size_t)NW * 16 * 8 * NT * 4; }
+    __host__ __device__ static size_t tiles_off(int nb) { return part_off(nb) + (size_t)NW * 16 * 8 * NT * 4; }
+    __host__ __device__ static size_t bytes(int nb) { return tiles_off(nb) + (size_t)NW * DEPTH * TILE_BYTES; }
 };
 
 // Quantise the B activation columns straight into B fragments (image layout as
@@ -164,48 +177,56 @@ __global__ void __launch_bounds__(256) mma_prep_kernel(const float* __restrict__
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// Weights of four consecutive blocks for a thread's two rows: code words and the
-// scales/mins as binary16 pairs (blocks 2i, 2i+1 of the step in word i).
-struct StepRegs {
-    uint32_t w0[4], w1[4];
-    uint32_t dA[2], dB[2], mA[2], mB[2];
-};
-
-__device__ __forceinline__ void load_step(StepRegs& r, const uint8_t* ca, const uint8_t* cb, const uint16_t* da,
-                                          const uint16_t* db, const uint16_t* ma, const uint16_t* mb, int b0) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        r.w0[j] = __ldg(reinterpret_cast<const unsigned int*>(ca + 16 * (b0 + j)));
-        r.w1[j] = __ldg(reinterpret_cast<const unsigned int*>(cb + 16 * (b0 + j)));
-    }
-    const uint2 a = __ldg(reinterpret_cast<const uint2*>(da + b0));
-    const uint2 b = __ldg(reinterpret_cast<const uint2*>(db + b0));
-    const uint2 c = __ldg(reinterpret_cast<const uint2*>(ma + b0));
-    const uint2 e = __ldg(reinterpret_cast<const uint2*>(mb + b0));
-    r.dA[0] = a.x; r.dA[1] = a.y;
-    r.dB[0] = b.x; r.dB[1] = b.y;
-    r.mA[0] = c.x; r.mA[1] = c.y;
-    r.mB[0] = e.x; r.mB[1] = e.y;
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// binary16 j (0..3) of a pair array, as float
-__device__ __forceinline__ float half_of(const uint32_t (&w)[2], int j) {
-    return half_bits_to_float((unsigned short)(w[j >> 1] >> (16 * (j & 1))));
+// Copies one tile (rows r0..r0+15 clamped to n, blocks blk0..blk0+7) into `tile` with
+// the warp's lanes: 128 code chunks of 16 B, 16 scale rows and 16 min rows of 16 B.
+__device__ __forceinline__ void issue_tile(const PlainParams& p, unsigned char* tile, int r0, int blk0, int lane) {
+    const int nb = p.k >> 5;
+    const size_t row_bytes = (size_t)(p.k >> 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        const int row = c >> 3, col = c & 7;
+        const int rr = min(r0 + row, p.n - 1);
+        cp_async16(tile + row * TILE_ROW + col * 16, p.lo + (size_t)rr * row_bytes + (size_t)(blk0 + col) * 16);
+    }
+    const int row = lane & 15;
+    const int rr = min(r0 + row, p.n - 1);
+    const uint16_t* plane = lane < 16 ? p.scale : p.min;
+    cp_async16(tile + TILE_CODES + (lane >> 4) * 256 + row * 16, plane + (size_t)rr * nb + blk0);
 }
 
 // The GEMV (kernel 2 of 2, or alone without a workspace).  With PREP the activation
 // image comes from the workspace in one bulk copy; without, every CTA quantises.
 template <int NT, bool PREP>
-__global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p, const unsigned char* img,
+__global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, const unsigned char* img,
                                                                  unsigned int* err) {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) uint64_t img_bar;
     const int nb = p.k >> 5;
-    const int QC = nb / KC;     // k chunks per row group (1, 2, 4 or 8)
-    const int RG = NW / QC;     // row groups per CTA pass
+    const int QC = nb / KC;  // warps per row group (k split): 2, 4 or 8
+    const int RG = NW / QC;  // row groups per CTA pass
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int my_rg = warp / QC, my_q = warp % QC;
+    const int n_groups = (p.n + 15) >> 4;
+    unsigned char* tiles = sm + Smem<NT>::tiles_off(nb) + (size_t)warp * DEPTH * TILE_BYTES;
+
+    // weights do not depend on earlier work: start the first tiles before waiting for it
+    auto group_of = [&](int pass) { return (blockIdx.x + pass * gridDim.x) * RG + my_rg; };
+#pragma unroll
+    for (int d = 0; d < DEPTH; ++d) {
+        if (group_of(d) < n_groups) issue_tile(p, tiles + d * TILE_BYTES, group_of(d) * 16, my_q * KC, lane);
+        cp_async_commit();
+    }
 
     pdl_wait();
     if (threadIdx.x == 0) pdl_launch_dependents();
@@ -238,6 +259,7 @@ __global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p, 
         // give up together if the copy never landed (bounded wait), leaving the error word set
         if (__syncthreads_or(ok == 0)) {
             if (threadIdx.x == 0) atomicOr(err, ERR_WAIT_FULL);
+            cp_async_wait<0>();
             return;
         }
     } else {
@@ -250,54 +272,51 @@ __global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p, 
     const float* Sv = reinterpret_cast<const float*>(sm + Smem<NT>::Sv_off(nb));
     float* part = reinterpret_cast<float*>(sm + Smem<NT>::part_off(nb));
 
-    const int n_groups = (p.n + 15) >> 4;
-    const size_t row_bytes = (size_t)(p.k >> 1);
-    for (int base = blockIdx.x * RG; base < n_groups; base += gridDim.x * RG) {
+    for (int pass = 0; (blockIdx.x + pass * gridDim.x) * RG < n_groups; ++pass) {
+        const int base = (blockIdx.x + pass * gridDim.x) * RG;
         const int grp = base + my_rg;
+        const unsigned char* tile = tiles + (pass % DEPTH) * TILE_BYTES;
+        cp_async_wait<DEPTH - 1>();
+        __syncwarp();
         float acc[NT][4];
 #pragma unroll
         for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
         if (grp < n_groups) {
-            const int ra = min(grp * 16 + g, p.n - 1), rb = min(grp * 16 + g + 8, p.n - 1);
-            const uint8_t* ca = p.lo + (size_t)ra * row_bytes + 4 * t;
-            const uint8_t* cb = p.lo + (size_t)rb * row_bytes + 4 * t;
-            const uint16_t* da = p.scale + (size_t)ra * nb;
-            const uint16_t* db = p.scale + (size_t)rb * nb;
-            const uint16_t* ma = p.min + (size_t)ra * nb;
-            const uint16_t* mb = p.min + (size_t)rb * nb;
-            // four steps of four blocks; the loads of step i+1 are in flight while step i computes
-            StepRegs buf[2];
-            load_step(buf[0], ca, cb, da, db, ma, mb, my_q * KC);
+            const unsigned short* dsc = reinterpret_cast<const unsigned short*>(tile + TILE_CODES);
+            const unsigned short* dmn = dsc + 128;
 #pragma unroll
-            for (int step = 0; step < KC / 4; ++step) {
-                if (step + 1 < KC / 4) load_step(buf[(step + 1) & 1], ca, cb, da, db, ma, mb, my_q * KC + 4 * (step + 1));
-                const StepRegs& cur = buf[step & 1];
+            for (int j = 0; j < KC; ++j) {
+                const int b = my_q * KC + j;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(tile + g * TILE_ROW + j * 16 + 4 * t);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + (g + 8) * TILE_ROW + j * 16 + 4 * t);
+                uint32_t alo[4], ahi[4];
+                a_frags(w0, w1, alo, ahi);
+                const float d0 = half_bits_to_float(dsc[g * 8 + j]), d1 = half_bits_to_float(dsc[(g + 8) * 8 + j]);
+                const float m0 = half_bits_to_float(dmn[g * 8 + j]), m1 = half_bits_to_float(dmn[(g + 8) * 8 + j]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int b = my_q * KC + 4 * step + j;
-                    uint32_t alo[4], ahi[4];
-                    a_frags(cur.w0[j], cur.w1[j], alo, ahi);
-                    const float d0 = half_of(cur.dA, j), d1 = half_of(cur.dB, j);
-                    const float m0 = half_of(cur.mA, j), m1 = half_of(cur.mB, j);
-#pragma unroll
-                    for (int tt = 0; tt < NT; ++tt) {
-                        const uint2 bl = frag[((b * 2 + 0) * NT + tt) * 32 + lane];
-                        const uint2 bh = frag[((b * 2 + 1) * NT + tt) * 32 + lane];
-                        float dl[4], D[4];
-                        mma_16816(dl, alo, bl.x, bl.y);
-                        mma_16816_acc(D, ahi, bh.x, bh.y, dl);  // exact integer block dots
-                        const float2 s2 = *reinterpret_cast<const float2*>(sv + b * 8 * NT + tt * 8 + 2 * t);
-                        const float2 S2 = *reinterpret_cast<const float2*>(Sv + b * 8 * NT + tt * 8 + 2 * t);
-                        // (row g, col 2t), (row g, col 2t+1), (row g+8, col 2t), (row g+8, col 2t+1)
-                        acc[tt][0] = fmaf(s2.x, fmaf(d0, D[0], m0 * S2.x), acc[tt][0]);
-                        acc[tt][1] = fmaf(s2.y, fmaf(d0, D[1], m0 * S2.y), acc[tt][1]);
-                        acc[tt][2] = fmaf(s2.x, fmaf(d1, D[2], m1 * S2.x), acc[tt][2]);
-                        acc[tt][3] = fmaf(s2.y, fmaf(d1, D[3], m1 * S2.y), acc[tt][3]);
-                    }
+                for (int tt = 0; tt < NT; ++tt) {
+                    const uint2 bl = frag[((b * 2 + 0) * NT + tt) * 32 + lane];
+                    const uint2 bh = frag[((b * 2 + 1) * NT + tt) * 32 + lane];
+                    float dl[4], D[4];
+                    mma_16816(dl, alo, bl.x, bl.y);
+                    mma_16816_acc(D, ahi, bh.x, bh.y, dl);  // exact integer block dots
+                    const float2 s2 = *reinterpret_cast<const float2*>(sv + b * 8 * NT + tt * 8 + 2 * t);
+                    const float2 S2 = *reinterpret_cast<const float2*>(Sv + b * 8 * NT + tt * 8 + 2 * t);
+                    // (row g, col 2t), (row g, col 2t+1), (row g+8, col 2t), (row g+8, col 2t+1)
+                    acc[tt][0] = fmaf(s2.x, fmaf(d0, D[0], m0 * S2.x), acc[tt][0]);
+                    acc[tt][1] = fmaf(s2.y, fmaf(d0, D[1], m0 * S2.y), acc[tt][1]);
+                    acc[tt][2] = fmaf(s2.x, fmaf(d1, D[2], m1 * S2.x), acc[tt][2]);
+                    acc[tt][3] = fmaf(s2.y, fmaf(d1, D[3], m1 * S2.y), acc[tt][3]);
                 }
             }
         }
-        // partial sums of the QC k-chunk warps of each row group meet in shared memory
+        __syncwarp();
+        // refill this slot with the tile of pass + DEPTH (an empty group keeps the count)
+        if (group_of(pass + DEPTH) < n_groups)
+            issue_tile(p, tiles + (pass % DEPTH) * TILE_BYTES, group_of(pass + DEPTH) * 16, my_q * KC, lane);
+        cp_async_commit();
+
+        // partial sums of the QC k-split warps of each row group meet in shared memory
         float* mine = part + (size_t)warp * 16 * 8 * NT;
 #pragma unroll
         for (int tt = 0; tt < NT; ++tt) {
@@ -307,7 +326,6 @@ __global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p, 
             mine[(g + 8) * 8 * NT + tt * 8 + 2 * t + 1] = acc[tt][3];
         }
         __syncthreads();
-        // RG row groups x 16 rows x batch columns, one output per thread per step
         for (int o = threadIdx.x; o < RG * 16 * 8 * NT; o += NW * 32) {
             const int rg = o / (16 * 8 * NT);
             const int rem = o - rg * 16 * 8 * NT;
@@ -321,13 +339,14 @@ __global__ void __launch_bounds__(NW * 32, 2) mma_batched_kernel(PlainParams p, 
         }
         __syncthreads();
     }
+    cp_async_wait<0>();
 }
 
 }  // namespace mma
 
 bool mma_supported(int bits, int k, int batch) {
     const int nb = k >> 5;
-    return bits == 4 && batch >= 8 && batch <= 16 && (nb == 16 || nb == 32 || nb == 64 || nb == 128);
+    return bits == 4 && batch >= 8 && batch <= 16 && (nb == 16 || nb == 32 || nb == 64);
 }
 
 size_t mma_workspace_bytes(int k, int batch) {
@@ -341,8 +360,9 @@ static int launch_mma_t(const PlainParams& p, unsigned char* ws, const LaunchCtx
     const int QC = nb / mma::KC, RG = mma::NW / QC;
     const int n_groups = (p.n + 15) >> 4;
     const size_t smem = mma::Smem<NT>::bytes(nb);
+    if (smem > (size_t)lc.max_smem_optin - 1024) return QG_ERR_UNSUPPORTED;
     int grid = (n_groups + RG - 1) / RG;
-    if (grid > lc.sm_count * 2) grid = lc.sm_count * 2;
+    if (grid > lc.sm_count) grid = lc.sm_count;
     if (grid < 1) grid = 1;
     if (!ws) {
         auto kern = mma::mma_batched_kernel<NT, false>;

@@ -68,6 +68,10 @@ def _load():
         lib.or_argmax_f32.restype = i64
         lib.or_wht.argtypes = [vp, i64, vp]
         lib.or_cq_matvec.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, vp, vp]
+        lib.or_logsumexp.argtypes = [vp, i64]
+        lib.or_logsumexp.restype = dbl
+        lib.or_select.argtypes = [vp, i64, vp, i64, vp]
+        lib.or_select.restype = i64
         _lib = lib
     return _lib
 
@@ -217,6 +221,25 @@ def cq_matvec(m: dict, x: np.ndarray, group: int, row_start: int = 0, row_count:
                          _p(_c(m["row_scale"], np.uint16)), k, group, row_start, row_count, _p(x), _p(y), _p(xw),
                          _p(uw))
     return y
+
+
+def logsumexp(v) -> float:
+    """log(sum(exp(v))) in fp64, NaN skipped."""
+    v = _c(np.atleast_1d(v), np.float64)
+    return float(_load().or_logsumexp(_p(v), v.size))
+
+
+def select(v, allowed=None):
+    """(id, logprob): the allowed id of the largest value (lowest id on ties) and
+    v[id] - logsumexp(v); allowed=None means every id.  id = -1 if none qualifies."""
+    v = _c(np.atleast_1d(v), np.float64)
+    lp = ctypes.c_double(0.0)
+    if allowed is None:
+        idx = _load().or_select(_p(v), v.size, None, 0, ctypes.byref(lp))
+    else:
+        a = _c(np.atleast_1d(allowed), np.int32)
+        idx = _load().or_select(_p(v), v.size, _p(a), a.size, ctypes.byref(lp))
+    return int(idx), float(lp.value)
 
 
 def normwise_error(y, ref) -> float:

@@ -252,3 +252,40 @@ void or_cq_matvec(const uint8_t* idx, const uint16_t* codebook, const uint16_t* 
         y[j] = or_half_to_double(row_scale[r]) * acc;
     }
 }
+
+/*
+ * log sum_i exp(v_i) over all n values, in fp64 (max-shifted).  The full-vocabulary
+ * normaliser of the selected token's log-probability (needle.js "Inference
+ * backends", "Resident layers": the selected ID is returned with its
+ * full-vocabulary log probability).  Reading: NaN values are skipped.
+ */
+double or_logsumexp(const double* v, int64_t n) {
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i)
+        if (!isnan(v[i]) && v[i] > m) m = v[i];
+    if (m == -INFINITY) return -INFINITY;
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        if (!isnan(v[i])) s += exp(v[i] - m);
+    return m + log(s);
+}
+
+/*
+ * Constrained selection (needle.js "Resident layers": grammar-allowed token IDs
+ * uploaded as an ascending list, the selected ID and its full-vocabulary log
+ * probability returned).  Reading: the selected ID is the allowed ID of the
+ * largest value, the lowest ID among equals, NaN never selected; allowed == NULL
+ * means every ID.  Returns the ID (-1 if nothing can be selected) and writes
+ * v[id] - logsumexp(v) to *logprob.
+ */
+int64_t or_select(const double* v, int64_t n, const int32_t* allowed, int64_t n_allowed, double* logprob) {
+    int64_t best = -1;
+    const int64_t cnt = allowed ? n_allowed : n;
+    for (int64_t j = 0; j < cnt; ++j) {
+        const int64_t id = allowed ? (int64_t)allowed[j] : j;
+        if (id < 0 || id >= n || isnan(v[id])) continue;
+        if (best < 0 || v[id] > v[best] || (v[id] == v[best] && id < best)) best = id;
+    }
+    *logprob = best < 0 ? NAN : v[best] - or_logsumexp(v, n);
+    return best;
+}

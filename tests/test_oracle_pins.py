@@ -385,3 +385,42 @@ def test_normwise_error_definition():
     rms = math.sqrt((1 + 4) / 4)
     y = ref + np.array([1e-4, 0.0, 2e-4, 0.0])
     assert math.isclose(oracle.normwise_error(y, ref), 2e-4 / rms, rel_tol=1e-12)
+
+
+# ------------------------------------------------------------------ constrained selection
+def test_logsumexp_closed_forms_and_scipy():
+    import scipy.special
+    assert math.isclose(oracle.logsumexp(np.zeros(1000)), math.log(1000), rel_tol=1e-15)
+    assert math.isclose(oracle.logsumexp(np.array([0.0, math.log(3.0)])), math.log(4.0), rel_tol=1e-15)
+    rng = np.random.default_rng(80)
+    v = rng.standard_normal(5000) * 7
+    assert math.isclose(oracle.logsumexp(v), float(scipy.special.logsumexp(v)), rel_tol=1e-13)
+    assert math.isclose(oracle.logsumexp(v + 1000.0), oracle.logsumexp(v) + 1000.0, rel_tol=1e-13)  # shift-invariant
+    assert oracle.logsumexp(np.array([np.nan, 2.0])) == 2.0
+
+
+def test_select_closed_forms():
+    n = 4096
+    idx, lp = oracle.select(np.zeros(n))
+    assert idx == 0 and math.isclose(lp, -math.log(n), rel_tol=1e-14)  # uniform: ties to the lowest id
+    v = np.zeros(8)
+    v[5] = math.log(3.0)
+    idx, lp = oracle.select(v)
+    assert idx == 5 and math.isclose(lp, math.log(3.0 / 10.0), rel_tol=1e-14)
+    idx, lp = oracle.select(v, [1, 2, 7])
+    assert idx == 1 and math.isclose(lp, math.log(1.0 / 10.0), rel_tol=1e-14)
+    assert oracle.select(v, [])[0] == -1
+
+
+def test_select_brute_force_and_probabilities_sum_to_one():
+    rng = np.random.default_rng(81)
+    for trial in range(20):
+        n = int(rng.integers(2, 3000))
+        v = np.round(rng.standard_normal(n) * 4, 1)  # repeats make ties likely
+        allowed = np.sort(rng.choice(n, size=int(rng.integers(1, n)), replace=False)).astype(np.int32)
+        idx, lp = oracle.select(v, allowed)
+        best = max(allowed.tolist(), key=lambda i: (v[i], -i))
+        assert idx == best
+        probs = np.exp(v - oracle.logsumexp(v))
+        assert math.isclose(probs.sum(), 1.0, rel_tol=1e-12)
+        assert math.isclose(math.exp(lp), probs[idx], rel_tol=1e-12)

@@ -159,6 +159,35 @@ int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const u
                          size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * Constrained selection over the vocabulary (needle.js "Inference backends",
+ * "Resident layers": the host uploads the grammar-allowed token IDs and reads back
+ * only the selected ID and its full-vocabulary log probability; the allowed-token
+ * argmax and log-softmax of its "selection" pass).
+ * qg_logits_select: over logits l[n] (device fp32),
+ *   token   = the allowed ID of the largest logit, the lowest ID among equal maxima,
+ *             NaN never selected; -1 if no allowed ID qualifies;
+ *   logprob = l[token] - log(sum_i exp(l[i])) over ALL n logits (NaN skipped);
+ *             NaN when token is -1.
+ *   allowed : device int32 [n_allowed] token IDs in any order (ascending as the page
+ *             has it; duplicates and IDs outside [0, n) are ignored), or NULL for all.
+ *   token : device int32 [1];  logprob : device fp32 [1] (written).
+ *   ws : device workspace of qg_select_workspace_bytes() bytes, zero-filled once after
+ *        allocation; every completed call leaves it zeroed.  Calls sharing a workspace
+ *        must not overlap on the GPU.
+ * vocab_softcap_select: vocab_softcap_argmax's soft-capped logits (written to `logits`,
+ * required here) followed by qg_logits_select on them, the second launch chained to
+ * the first by programmatic dependent launch; ws holds qg_vocab_select_workspace_bytes().
+ */
+size_t qg_select_workspace_bytes(void);
+int qg_logits_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token,
+                     float* logprob, void* ws, size_t ws_bytes, unsigned flags, void* stream);
+size_t qg_vocab_select_workspace_bytes(void);
+int vocab_softcap_select(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
+                         int n_vocab, int k, const float* x, float softcap, const int32_t* allowed, int n_allowed,
+                         float* logits, int32_t* token, float* logprob, void* ws, size_t ws_bytes, unsigned flags,
+                         void* stream);
+
+/*
  * Grouped GEMV: `count` independent GEMVs of one weight format in two launches
  * (needle.js "Inference backends", "Hybrid GPU execution": independent projections
  * batched into one dispatch over a combined weight arena; genie-ai-runtime,

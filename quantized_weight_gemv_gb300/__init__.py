@@ -40,6 +40,11 @@ SIGNATURES = {
     "cq_fwht_matvec": (_i, [_u8p, _u16p, _u16p, _i, _i, _i, _i, _i, _f32p, _f32p, _u, _vp]),
     "qg_vocab_workspace_bytes": (_sz, []),
     "vocab_softcap_argmax": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _f32p, _f, _f32p, _i32p, _vp, _sz, _u, _vp]),
+    "qg_select_workspace_bytes": (_sz, []),
+    "qg_logits_select": (_i, [_f32p, _i, _i32p, _i, _i32p, _f32p, _vp, _sz, _u, _vp]),
+    "qg_vocab_select_workspace_bytes": (_sz, []),
+    "vocab_softcap_select": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _f32p, _f, _i32p, _i, _f32p, _i32p, _f32p, _vp,
+                                  _sz, _u, _vp]),
     "qg_grouped_workspace_bytes": (_sz, [_vp, _i]),
     "qgemv_grouped": (_i, [_i, _vp, _i, _vp, _sz, _u, _vp]),
     "qgemv_grouped_noalloc": (_i, [_i, _vp, _i, _u, _vp]),
@@ -290,6 +295,59 @@ def qgemv_grouped(bits, mats, xs, ys, flags: int = 0):
     """One-shot :class:`GroupedGemv` call; returns ``ys``."""
     GroupedGemv(bits, mats, xs, ys, flags).run()
     return ys
+
+
+def select_workspace(device) -> torch.Tensor:
+    """A zero-filled workspace for :func:`qg_logits_select` (reusable; calls leave it zeroed)."""
+    return torch.zeros(int(lib().qg_select_workspace_bytes()), dtype=torch.uint8, device=device)
+
+
+def qg_logits_select(logits, allowed=None, token=None, logprob=None, ws=None, flags: int = 0):
+    """(token int32[1], logprob fp32[1]): the allowed ID of the largest logit and its
+    full-vocabulary log-probability; ``allowed`` is an int32 device tensor of IDs or None."""
+    _need(logits, "logits", _F32)
+    dev = logits.device
+    if allowed is not None:
+        _need(allowed, "allowed", (torch.int32,), dev)
+    token = torch.empty(1, dtype=torch.int32, device=dev) if token is None else token
+    logprob = torch.empty(1, dtype=torch.float32, device=dev) if logprob is None else logprob
+    ws = select_workspace(dev) if ws is None else ws
+    with torch.cuda.device(dev):
+        _check(lib().qg_logits_select(_ptr(logits), logits.numel(), _ptr(allowed),
+                                      0 if allowed is None else allowed.numel(), _ptr(token), _ptr(logprob), _ptr(ws),
+                                      ws.numel() * ws.element_size(), flags, _stream(dev)), "qg_logits_select")
+    return token, logprob
+
+
+def vocab_select_workspace(device) -> torch.Tensor:
+    """A zero-filled workspace for :func:`vocab_softcap_select`."""
+    return torch.zeros(int(lib().qg_vocab_select_workspace_bytes()), dtype=torch.uint8, device=device)
+
+
+def vocab_softcap_select(bits, lo, hi, scale, min, x, softcap: float = 30.0, allowed=None, logits=None, token=None,
+                         logprob=None, ws=None, flags: int = 0):
+    """(logits, token, logprob) of the soft-capped vocabulary projection with constrained selection."""
+    _need(lo, "lo", _U8)
+    dev = lo.device
+    if bits == 6:
+        _need(hi, "hi", _U8, dev)
+    for t, nm in ((scale, "scale"), (min, "min")):
+        _need(t, nm, _H16, dev)
+    _need(x, "x", _F32, dev)
+    if allowed is not None:
+        _need(allowed, "allowed", (torch.int32,), dev)
+    n, k = lo.shape[0], lo.shape[1] * 2
+    logits = torch.empty(n, dtype=torch.float32, device=dev) if logits is None else logits
+    token = torch.empty(1, dtype=torch.int32, device=dev) if token is None else token
+    logprob = torch.empty(1, dtype=torch.float32, device=dev) if logprob is None else logprob
+    ws = vocab_select_workspace(dev) if ws is None else ws
+    with torch.cuda.device(dev):
+        _check(lib().vocab_softcap_select(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min), n,
+                                          k, _ptr(x), float(softcap), _ptr(allowed),
+                                          0 if allowed is None else allowed.numel(), _ptr(logits), _ptr(token),
+                                          _ptr(logprob), _ptr(ws), ws.numel() * ws.element_size(), flags,
+                                          _stream(dev)), "vocab_softcap_select")
+    return logits, token, logprob
 
 
 def qg_quantize_act(x):

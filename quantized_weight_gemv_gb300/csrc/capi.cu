@@ -223,6 +223,42 @@ int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const u
     return launch_plain(pp, bits, EPI_ARGMAX, lc);
 }
 
+size_t qg_select_workspace_bytes(void) { return sizeof(SelectWorkspace); }
+
+int qg_logits_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token,
+                     float* logprob, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+    if (n < 1 || !logits || !token || !logprob) return QG_ERR_INVALID_ARG;
+    if (allowed && n_allowed < 0) return QG_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < sizeof(SelectWorkspace)) return QG_ERR_WORKSPACE;
+    if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    int rc = resolve(stream, flags, lc);
+    if (rc != QG_OK) return rc;
+    return launch_select(logits, n, allowed, allowed ? n_allowed : 0, token, logprob,
+                         reinterpret_cast<SelectWorkspace*>(ws), lc);
+}
+
+size_t qg_vocab_select_workspace_bytes(void) { return sizeof(VocabWorkspace) + sizeof(SelectWorkspace); }
+
+int vocab_softcap_select(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
+                         int n_vocab, int k, const float* x, float softcap, const int32_t* allowed, int n_allowed,
+                         float* logits, int32_t* token, float* logprob, void* ws, size_t ws_bytes, unsigned flags,
+                         void* stream) {
+    if (!logits || !token || !logprob) return QG_ERR_INVALID_ARG;
+    if (allowed && n_allowed < 0) return QG_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < qg_vocab_select_workspace_bytes()) return QG_ERR_WORKSPACE;
+    if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
+    unsigned char* w = reinterpret_cast<unsigned char*>(ws);
+    SelectWorkspace* sw = reinterpret_cast<SelectWorkspace*>(w + sizeof(VocabWorkspace));
+    // 1. the soft-capped logits (its unconstrained argmax goes to the workspace's scratch word)
+    int rc = vocab_softcap_argmax(bits, lo, hi, scale, min, n_vocab, k, x, softcap, logits, &sw->scratch_index, w,
+                                  sizeof(VocabWorkspace), flags, stream);
+    if (rc != QG_OK) return rc;
+    // 2. the selection, chained by programmatic dependent launch
+    return qg_logits_select(logits, n_vocab, allowed, n_allowed, token, logprob, sw, sizeof(SelectWorkspace),
+                            flags | QG_FLAG_PDL, stream);
+}
+
 size_t qg_grouped_workspace_bytes(const qg_gemv_desc* descs, int count) {
     if (!descs || count <= 0 || count > QG_MAX_GROUP) return 0;
     return grouped_workspace_bytes(descs, count);

@@ -267,6 +267,20 @@ struct VocabWorkspace {
     ArgmaxPartial part[VOCAB_MAX_CTAS];
 };
 
+// Workspace of the constrained selection: a counter, then one partial per CTA holding
+// an online log-sum-exp (max m, sum of exp(l - m)) and a best (value, index).
+constexpr int SELECT_MAX_CTAS = 1024;
+struct SelectPartial {
+    float m, s, bv;
+    int bi;
+};
+struct SelectWorkspace {
+    unsigned int counter;
+    int scratch_index;  // the unconstrained argmax of the vocabulary kernel, unused afterwards
+    unsigned int pad[62];
+    SelectPartial part[SELECT_MAX_CTAS];
+};
+
 // Block-wide (value, index) reduction, then the last CTA to finish reduces every
 // CTA's partial, writes the index and re-arms the counter.  No CTA waits on another.
 // Called by all threads of the block.

@@ -1,0 +1,130 @@
+// Constrained token selection over a logit vector.
+//
+// needle.js "Inference backends", "Resident layers": tool calling uploads an
+// ascending list of grammar-allowed token IDs and reads back only the selected ID
+// and its full-vocabulary log probability.  Here one pass over the logits does both
+// halves: every CTA folds its share of the logits into an online log-sum-exp
+// (running max m and sum of exp(l - m)) and its share of the allowed IDs into a
+// (value, lowest ID) best; the last CTA to finish merges all partials, writes the
+// selected ID and l[id] - logsumexp(l), and re-arms the counter.  No CTA waits on
+// another.
+#include "qg_internal.h"
+
+namespace qg {
+
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    if (m2 == -INFINITY) return;
+    if (m == -INFINITY) {
+        m = m2;
+        s = s2;
+        return;
+    }
+    const float M = fmaxf(m, m2);
+    s = s * expf(m - M) + s2 * expf(m2 - M);
+    m = M;
+}
+
+__device__ __forceinline__ void select_warp_reduce(float& m, float& s, float& bv, int& bi) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        lse_merge(m, s, m2, s2);
+        if (better(v2, i2, bv, bi)) {
+            bv = v2;
+            bi = i2;
+        }
+    }
+}
+
+// block-wide merge of (m, s, bv, bi); the result is valid in thread 0
+__device__ __forceinline__ void select_block_reduce(float& m, float& s, float& bv, int& bi, SelectPartial* sred) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    select_warp_reduce(m, s, bv, bi);
+    __syncthreads();
+    if (lane == 0) sred[wid] = SelectPartial{m, s, bv, bi};
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < nw; ++w) {
+            lse_merge(m, s, sred[w].m, sred[w].s);
+            if (better(sred[w].bv, sred[w].bi, bv, bi)) {
+                bv = sred[w].bv;
+                bi = sred[w].bi;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ logits, int n,
+                                                     const int32_t* __restrict__ allowed, int n_allowed,
+                                                     int32_t* token, float* logprob, SelectWorkspace* ws) {
+    __shared__ SelectPartial sred[8];
+    __shared__ int last;
+    pdl_wait();  // the logits come from the preceding kernel
+    if (threadIdx.x == 0) pdl_launch_dependents();
+
+    // log-sum-exp over this CTA's rows (NaN skipped)
+    const long long r0 = (long long)blockIdx.x * n / gridDim.x, r1 = (long long)(blockIdx.x + 1) * n / gridDim.x;
+    float m = -INFINITY, s = 0.0f;
+    for (long long i = r0 + threadIdx.x; i < r1; i += blockDim.x) {
+        const float v = logits[i];
+        if (v == v) lse_merge(m, s, v, 1.0f);
+    }
+    // best allowed (value, lowest id) over this CTA's share of the allowed list
+    float bv = __int_as_float(0x7fc00000);
+    int bi = 0x7fffffff;
+    const long long cnt = allowed ? n_allowed : n;
+    const long long a0 = (long long)blockIdx.x * cnt / gridDim.x, a1 = (long long)(blockIdx.x + 1) * cnt / gridDim.x;
+    for (long long j = a0 + threadIdx.x; j < a1; j += blockDim.x) {
+        const long long id = allowed ? (long long)allowed[j] : j;
+        if (id < 0 || id >= n) continue;
+        const float v = logits[id];
+        if (better(v, (int)id, bv, bi)) {
+            bv = v;
+            bi = (int)id;
+        }
+    }
+    select_block_reduce(m, s, bv, bi, sred);
+    if (threadIdx.x == 0) {
+        ws->part[blockIdx.x] = SelectPartial{m, s, bv, bi};
+        __threadfence();
+        last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    m = -INFINITY;
+    s = 0.0f;
+    bv = __int_as_float(0x7fc00000);
+    bi = 0x7fffffff;
+    for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+        const float cm = __ldcg(&ws->part[c].m), cs = __ldcg(&ws->part[c].s);
+        const float cv = __ldcg(&ws->part[c].bv);
+        const int ci = __ldcg(&ws->part[c].bi);
+        lse_merge(m, s, cm, cs);
+        if (better(cv, ci, bv, bi)) {
+            bv = cv;
+            bi = ci;
+        }
+    }
+    select_block_reduce(m, s, bv, bi, sred);
+    if (threadIdx.x == 0) {
+        const bool found = bi != 0x7fffffff;
+        *token = found ? bi : -1;
+        *logprob = found ? bv - (m + logf(s)) : __int_as_float(0x7fc00000);
+        ws->counter = 0u;
+    }
+}
+
+int launch_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token, float* logprob,
+                  SelectWorkspace* ws, const LaunchCtx& lc) {
+    long long grid = ((long long)n + 8191) / 8192;
+    if (grid > lc.sm_count) grid = lc.sm_count;
+    if (grid > SELECT_MAX_CTAS) grid = SELECT_MAX_CTAS;
+    if (grid < 1) grid = 1;
+    return launch_kernel(select_kernel, dim3((unsigned)grid), dim3(256), 0, lc, logits, n, allowed, n_allowed, token,
+                         logprob, ws);
+}
+
+}  // namespace qg

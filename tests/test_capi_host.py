@@ -150,3 +150,20 @@ def test_grouped_validation(lib):
     assert f(4, ctypes.cast(bad, ctypes.c_void_p), 1, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
     empty = (D * 1)(D(None, None, None, None, None, None, 0, 2048))
     assert f(4, ctypes.cast(empty, ctypes.c_void_p), 1, None, 0, 0, None) == qg.QG_OK
+
+
+def test_select_validation(lib):
+    f = lib.qg_logits_select
+    ws = lib.qg_select_workspace_bytes()
+    assert ws >= 256 + 16 * 152
+    assert f(A16, 0, None, 0, A16, A16, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(None, 8, None, 0, A16, A16, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(A16, 8, A16, -1, A16, A16, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(A16, 8, None, 0, A16, A16, A16, ws - 1, 0, None) == qg.QG_ERR_WORKSPACE
+    assert f(A16, 8, None, 0, A16, A16, MIS, ws, 0, None) == qg.QG_ERR_ALIGNMENT
+    g = lib.vocab_softcap_select
+    vws = lib.qg_vocab_select_workspace_bytes()
+    assert vws == lib.qg_vocab_workspace_bytes() + ws
+    assert g(6, A16, A16, A16, A16, 8, 64, A16, 30.0, None, 0, None, A16, A16, A16, vws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert g(6, A16, A16, A16, A16, 8, 64, A16, 30.0, None, 0, A16, A16, A16, A16, vws - 1, 0, None) == qg.QG_ERR_WORKSPACE
+    assert g(3, A16, A16, A16, A16, 8, 64, A16, 30.0, None, 0, A16, A16, A16, A16, vws, 0, None) == qg.QG_ERR_UNSUPPORTED

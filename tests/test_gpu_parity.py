@@ -359,3 +359,65 @@ def test_batched_tensor_core_with_and_without_workspace(batch, k):
         Y = qg.qgemv_batched(4, wd["lo"], None, wd["scale"], wd["min"], Xt, ws=ws).cpu().numpy()
         for b in range(batch):
             assert_close(Y[b], refs[b])
+
+
+# ---------------------------------------------------------------- constrained selection
+def _allowed_cases(n, rng):
+    yield None
+    yield np.sort(rng.choice(n, size=max(1, n // 100), replace=False)).astype(np.int32)
+    yield np.array([n - 1], np.int32)
+    yield np.array([3, 3, -5, n + 7, 1], np.int32)  # duplicates and out-of-range IDs are ignored
+    yield np.arange(n, dtype=np.int32)
+
+
+@pytest.mark.parametrize("n", [1, 1000, 262144])
+def test_logits_select(n):
+    rng = np.random.default_rng(n)
+    logits = (rng.standard_normal(n) * 5).astype(np.float32)
+    logits[rng.integers(0, n, size=min(n, 50))] = np.float32(2.5)  # exact ties
+    lt = torch.from_numpy(logits).to(DEV)
+    ws = qg.select_workspace(DEV)
+    for allowed in _allowed_cases(n, rng):
+        at = None if allowed is None else torch.from_numpy(allowed).to(DEV)
+        tok, lp = qg.qg_logits_select(lt, at, ws=ws)
+        ref_tok, ref_lp = oracle.select(logits.astype(np.float64), allowed)
+        assert int(tok.item()) == ref_tok
+        if ref_tok < 0:
+            assert np.isnan(float(lp.item()))  # nothing selectable
+        else:
+            assert abs(float(lp.item()) - ref_lp) <= TOL * max(1.0, abs(ref_lp))
+    assert int(ws[:4].view(torch.int32).item()) == 0  # the completion counter is re-armed
+
+
+def test_logits_select_nothing_allowed():
+    lt = torch.randn(100, device=DEV)
+    tok, lp = qg.qg_logits_select(lt, torch.tensor([200, -1], dtype=torch.int32, device=DEV))
+    assert int(tok.item()) == -1 and np.isnan(float(lp.item()))
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_vocab_softcap_select(bits):
+    n, k = 40000, 2048
+    w = datagen.make_quantized(bits, 66, n, k)
+    x = datagen.normal_f32(66, 1, k)
+    wd = dev_w(w)
+    xt = torch.from_numpy(x).to(DEV)
+    ref_l = oracle.softcap(oracle_gemv_par(w, x), 30.0)
+    rng = np.random.default_rng(67)
+    ws = qg.vocab_select_workspace(DEV)
+    for allowed in (None, np.sort(rng.choice(n, size=500, replace=False)).astype(np.int32)):
+        at = None if allowed is None else torch.from_numpy(allowed).to(DEV)
+        for flags in (0, qg.QG_FLAG_PDL):
+            logits, tok, lp = qg.vocab_softcap_select(bits, wd["lo"], wd.get("hi"), wd["scale"], wd["min"], xt, 30.0,
+                                                      allowed=at, ws=ws, flags=flags)
+            l = logits.cpu().numpy()
+            assert_close(l, ref_l)
+            # exact against the GPU's own logits; against the oracle's when the margin clears the tolerance
+            own_tok, _ = oracle.select(l.astype(np.float64), allowed)
+            assert int(tok.item()) == own_tok
+            ref_tok, ref_lp = oracle.select(ref_l, allowed)
+            cand = ref_l if allowed is None else ref_l[allowed]
+            top2 = np.sort(cand)[-2:]
+            if top2[1] - top2[0] > 2 * TOL * max(abs(top2[1]), float(np.sqrt(np.mean(ref_l ** 2)))):
+                assert int(tok.item()) == ref_tok
+            assert abs(float(lp.item()) - ref_lp) <= TOL * max(1.0, abs(ref_lp))

@@ -63,6 +63,7 @@ def _load():
         lib.dg_f32_to_f16.argtypes = [vp, i64, vp]
         lib.dg_pack_q4_codes.argtypes = [vp, i64, i64, vp]
         lib.dg_pack_q6_codes.argtypes = [vp, i64, i64, vp, vp]
+        lib.dg_pack_q2_codes.argtypes = [vp, i64, i64, vp]
         lib.dg_quantize_matrix.argtypes = [ctypes.c_int, vp, i64, i64, vp, vp, vp, vp]
         lib.dg_make_quantized.argtypes = [ctypes.c_int, u64, u64, i64, i64, dbl, vp, vp, vp, vp, ctypes.c_int]
         lib.dg_make_quantized.restype = ctypes.c_int
@@ -135,29 +136,42 @@ def pack_q6_codes(q: np.ndarray):
     return lo, hi
 
 
+def pack_q2_codes(q: np.ndarray) -> np.ndarray:
+    """Pack codes (uint8 [n][k], values 0..3) into the Q2 byte layout [n][k/4]."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    n, k = q.shape
+    assert k % 32 == 0
+    codes = np.empty((n, k // 4), dtype=np.uint8)
+    _load().dg_pack_q2_codes(_p(q), n, k, _p(codes))
+    return codes
+
+
+def _alloc_planes(bits: int, n: int, k: int):
+    if bits == 2:
+        return np.empty((n, k // 4), np.uint8), None, np.empty((n, k // 32), np.uint16), None
+    lo = np.empty((n, k // 2), dtype=np.uint8)
+    hi = np.empty((n, k // 4), dtype=np.uint8) if bits == 6 else None
+    return lo, hi, np.empty((n, k // 32), dtype=np.uint16), np.empty((n, k // 32), dtype=np.uint16)
+
+
 def quantize_matrix(bits: int, w: np.ndarray) -> dict:
     """Block-quantise a caller-supplied fp32 matrix [n][k] to the Q4 / Q6 layout."""
     w = np.ascontiguousarray(w, dtype=np.float32)
     n, k = w.shape
-    assert bits in (4, 6) and k % 32 == 0
-    lo = np.empty((n, k // 2), dtype=np.uint8)
-    hi = np.empty((n, k // 4), dtype=np.uint8) if bits == 6 else None
-    scale = np.empty((n, k // 32), dtype=np.uint16)
-    mn = np.empty((n, k // 32), dtype=np.uint16)
-    _load().dg_quantize_matrix(bits, _p(w), n, k, _p(lo), _p(hi) if hi is not None else None, _p(scale), _p(mn))
+    assert bits in (2, 4, 6) and k % 32 == 0
+    lo, hi, scale, mn = _alloc_planes(bits, n, k)
+    _load().dg_quantize_matrix(bits, _p(w), n, k, _p(lo), _p(hi) if hi is not None else None, _p(scale),
+                               _p(mn) if mn is not None else None)
     return {"bits": bits, "n": n, "k": k, "lo": lo, "hi": hi, "scale": scale, "min": mn}
 
 
 def make_quantized(bits: int, seed: int, n: int, k: int, sigma: float = 0.02, stream: int = STREAM_W,
                    nthreads: int | None = None) -> dict:
     """Seeded matrix W[r][c] = f32(sigma * normal(seed, stream, r*k + c)), block-quantised."""
-    assert bits in (4, 6) and k % 32 == 0
-    lo = np.empty((n, k // 2), dtype=np.uint8)
-    hi = np.empty((n, k // 4), dtype=np.uint8) if bits == 6 else None
-    scale = np.empty((n, k // 32), dtype=np.uint16)
-    mn = np.empty((n, k // 32), dtype=np.uint16)
+    assert bits in (2, 4, 6) and k % 32 == 0
+    lo, hi, scale, mn = _alloc_planes(bits, n, k)
     rc = _load().dg_make_quantized(bits, seed, stream, n, k, sigma, _p(lo), _p(hi) if hi is not None else None,
-                                   _p(scale), _p(mn), nthreads or _threads())
+                                   _p(scale), _p(mn) if mn is not None else None, nthreads or _threads())
     assert rc == 0
     return {"bits": bits, "n": n, "k": k, "lo": lo, "hi": hi, "scale": scale, "min": mn}
 

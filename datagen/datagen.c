@@ -28,11 +28,17 @@
  *       hi u8 [N][K/4], 8 bytes per block, byte t (0..7) holding the top 2
  *       code bits of codes t, t+8, t+16, t+24 in bits 0-1, 2-3, 4-5, 6-7.
  *   A weight decodes as  w = scale * code + min.
+ *   Q2: codes u8 [N][K/4], 8 bytes per block, byte t (0..7) holding codes t, t+8,
+ *       t+16, t+24 in bits 0-1, 2-3, 4-5, 6-7; scale f16 [N][K/32]; no min plane:
+ *       a weight decodes as w = scale * (code - 2) (zero point 2).
  * Asymmetric block quantiser used to make the packed inputs: lo = min(w),
  * hi = max(w) over the block; d = (hi - lo) / qmax in float (qmax 15 or 63);
  * scale = f16(d), min = f16(lo) (round to nearest even);
  * code = clamp(rint((w - min) / scale), 0, qmax) in float with the stored
  * half values; code = 0 when scale == 0.
+ * Q2 quantiser: scale = f16(max(hi, -lo / 2)) so that the codes 0..3 (values
+ * -2, -1, 0, 1 times the scale) cover the block; code = clamp(rint(w / scale) + 2,
+ * 0, 3) in float with the stored half; code = 2 when scale == 0.
  *   CQ: idx u8 [N][K/2]; element 2j in bits 0-3 of byte j, element 2j+1 in
  *       bits 4-7; codebook f16 [16]; row scale f16 [N].
  */
@@ -163,6 +169,39 @@ static void pack_q6_block(const uint8_t* q, uint8_t* lo16, uint8_t* hi8) {
                            (((q[t + 24] >> 4) & 3) << 6));
 }
 
+static void quantize_block_q2(const float* w, uint8_t* q, uint16_t* scale_bits) {
+    float lo = w[0], hi = w[0];
+    for (int i = 1; i < 32; ++i) {
+        if (w[i] < lo) lo = w[i];
+        if (w[i] > hi) hi = w[i];
+    }
+    float d = hi > -lo / 2.0f ? hi : -lo / 2.0f;
+    if (d < 0.0f) d = 0.0f;
+    uint16_t db = f32_to_f16_bits(d);
+    float d16 = f16_bits_to_f32(db);
+    for (int i = 0; i < 32; ++i) {
+        int c = 2;
+        if (d16 != 0.0f) {
+            float t = rintf(w[i] / d16) + 2.0f;
+            if (t < 0.0f) t = 0.0f;
+            if (t > 3.0f) t = 3.0f;
+            c = (int)t;
+        }
+        q[i] = (uint8_t)c;
+    }
+    *scale_bits = db;
+}
+
+static void pack_q2_block(const uint8_t* q, uint8_t* c8) {
+    for (int t = 0; t < 8; ++t)
+        c8[t] = (uint8_t)((q[t] & 3) | ((q[t + 8] & 3) << 2) | ((q[t + 16] & 3) << 4) | ((q[t + 24] & 3) << 6));
+}
+
+void dg_pack_q2_codes(const uint8_t* q, int64_t n, int64_t k, uint8_t* codes) {
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < k / 32; ++b) pack_q2_block(q + r * k + b * 32, codes + r * (k / 4) + b * 8);
+}
+
 /* Pack caller-chosen codes (values 0..15 / 0..63) for [n][k]; used by tests to
  * build exact cases.  q is row-major [n][k]. */
 void dg_pack_q4_codes(const uint8_t* q, int64_t n, int64_t k, uint8_t* codes) {
@@ -184,6 +223,11 @@ void dg_quantize_matrix(int bits, const float* w, int64_t n, int64_t k, uint8_t*
     int64_t nb = k / 32;
     for (int64_t r = 0; r < n; ++r) {
         for (int64_t b = 0; b < nb; ++b) {
+            if (bits == 2) {
+                quantize_block_q2(w + r * k + b * 32, q, scale + r * nb + b);
+                pack_q2_block(q, lo + r * (k / 4) + b * 8);
+                continue;
+            }
             quantize_block(w + r * k + b * 32, qmax, q, scale + r * nb + b, min + r * nb + b);
             if (bits == 4)
                 pack_q4_block(q, lo + r * (k / 2) + b * 16);
@@ -226,6 +270,11 @@ static void* qjob_run(void* arg) {
     for (int64_t r = j->row0; r < j->row1; ++r) {
         weights_row(j->key, r, j->k, j->sigma, row);
         for (int64_t b = 0; b < nb; ++b) {
+            if (j->bits == 2) {
+                quantize_block_q2(row + b * 32, q, j->scale + r * nb + b);
+                pack_q2_block(q, j->lo + r * (j->k / 4) + b * 8);
+                continue;
+            }
             quantize_block(row + b * 32, qmax, q, j->scale + r * nb + b, j->min + r * nb + b);
             if (j->bits == 4)
                 pack_q4_block(q, j->lo + r * (j->k / 2) + b * 16);
@@ -241,7 +290,7 @@ static void* qjob_run(void* arg) {
  * Returns 0 on success. */
 int dg_make_quantized(int bits, uint64_t seed, uint64_t stream, int64_t n, int64_t k, double sigma, uint8_t* lo,
                       uint8_t* hi, uint16_t* scale, uint16_t* min, int nthreads) {
-    if ((bits != 4 && bits != 6) || k % 32 != 0 || n < 0) return -1;
+    if ((bits != 2 && bits != 4 && bits != 6) || k % 32 != 0 || n < 0) return -1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     if (n < (int64_t)nthreads * 4) nthreads = 1;

@@ -54,6 +54,8 @@ def _load():
         lib.or_q4_code.restype = c_int
         lib.or_q6_code.argtypes = [vp, vp, i64]
         lib.or_q6_code.restype = c_int
+        lib.or_q2_code.argtypes = [vp, i64]
+        lib.or_q2_code.restype = c_int
         lib.or_codes.argtypes = [c_int, vp, vp, i64, i64, i64, vp]
         lib.or_dequant_rows.argtypes = [c_int, vp, vp, vp, vp, i64, i64, i64, vp]
         lib.or_blockdots.argtypes = [c_int, vp, vp, i64, i64, vp, vp]
@@ -106,7 +108,8 @@ def quantize_act(x: np.ndarray):
 def _planes(w: dict):
     lo = _c(w["lo"], np.uint8)
     hi = _c(w["hi"], np.uint8) if w["bits"] == 6 else None
-    return lo, hi, _c(w["scale"], np.uint16), _c(w["min"], np.uint16)
+    mn = _c(w["min"], np.uint16) if w["bits"] != 2 else None  # Q2: zero point 2, no min plane
+    return lo, hi, _c(w["scale"], np.uint16), mn
 
 
 def codes(w: dict, row0: int = 0, nrows: int | None = None) -> np.ndarray:

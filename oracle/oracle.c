@@ -14,6 +14,9 @@
  *       (r, 8*b + t) holding the top 2 bits of codes 32*b + t, +8, +16, +24
  *       in bits 0-1, 2-3, 4-5, 6-7.
  *   scale / min: one IEEE binary16 per block; a weight is scale*code + min.
+ *   Q2: codes byte (r, 8*b + t) holds the 2-bit codes 32*b + t, +8, +16, +24 in bits
+ *       0-1, 2-3, 4-5, 6-7; one binary16 scale per block, no min: a weight is
+ *       scale*(code - 2), the int2 zero point 2 of the Gemma WebGPU Engine ("Roadmap").
  *   CQ: byte (r, j) holds index 2j in bits 0-3 and index 2j+1 in bits 4-7.
  *
  * Where the pages leave a step open, the reading taken is stated at the
@@ -94,7 +97,14 @@ int or_q6_code(const uint8_t* row_lo, const uint8_t* row_hi, int64_t i) {
     return low | (high << 4);
 }
 
+/* code i of one Q2 row */
+int or_q2_code(const uint8_t* row_codes, int64_t i) {
+    int64_t b = i / 32, e = i % 32;
+    return (row_codes[8 * b + (e % 8)] >> (2 * (e / 8))) & 3;
+}
+
 static int code_at(int bits, const uint8_t* lo, const uint8_t* hi, int64_t k, int64_t r, int64_t i) {
+    if (bits == 2) return or_q2_code(lo + r * (k / 4), i);
     if (bits == 4) return or_q4_code(lo + r * (k / 2), i);
     return or_q6_code(lo + r * (k / 2), hi + r * (k / 4), i);
 }
@@ -113,6 +123,10 @@ void or_dequant_rows(int bits, const uint8_t* lo, const uint8_t* hi, const uint1
         int64_t rr = row0 + r;
         for (int64_t i = 0; i < k; ++i) {
             double d = or_half_to_double(scale[rr * nb + i / 32]);
+            if (bits == 2) {
+                out[r * k + i] = d * (double)(code_at(bits, lo, hi, k, rr, i) - 2);
+                continue;
+            }
             double m = or_half_to_double(min[rr * nb + i / 32]);
             out[r * k + i] = d * (double)code_at(bits, lo, hi, k, rr, i) + m;
         }
@@ -153,8 +167,9 @@ void or_gemv(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* sca
         double acc = 0.0;
         for (int64_t i = 0; i < k; ++i) {
             double d = or_half_to_double(scale[rr * nb + i / 32]);
-            double m = or_half_to_double(min[rr * nb + i / 32]);
-            double w = d * (double)code_at(bits, lo, hi, k, rr, i) + m;
+            double w = bits == 2 ? d * (double)(code_at(bits, lo, hi, k, rr, i) - 2)
+                                 : d * (double)code_at(bits, lo, hi, k, rr, i) +
+                                       or_half_to_double(min[rr * nb + i / 32]);
             double xd = (double)s_work[i / 32] * (double)xq_work[i];
             acc += w * xd;
         }

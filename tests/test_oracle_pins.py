@@ -424,3 +424,55 @@ def test_select_brute_force_and_probabilities_sum_to_one():
         probs = np.exp(v - oracle.logsumexp(v))
         assert math.isclose(probs.sum(), 1.0, rel_tol=1e-12)
         assert math.isclose(math.exp(lp), probs[idx], rel_tol=1e-12)
+
+
+# ------------------------------------------------------------------ 2-bit codes, zero point 2
+def test_q2_block_golden():
+    g = G.load("q2_block.txt")
+    codes = G.ints(g["codes"])
+    packed = np.array(G.hexbytes(g["bytes"]), np.uint8)[None, :]
+    from tests._layout import pack_q2
+    assert np.array_equal(pack_q2(np.array([codes])), packed)
+    assert np.array_equal(datagen.pack_q2_codes(np.array([codes], np.uint8)), packed)
+    w = {"bits": 2, "n": 1, "k": 32, "lo": packed, "hi": None, "scale": f16_bits([[G.floats(g["gemv.scale"])[0]]]),
+         "min": None}
+    assert oracle.codes(w)[0].tolist() == codes
+    y = oracle.gemv(w, np.ones(32, np.float32))
+    assert math.isclose(y[0], G.floats(g["gemv.y"])[0], rel_tol=1e-6)
+
+
+def test_q2_codes_dequant_and_dots():
+    rng = np.random.default_rng(90)
+    n, k = 6, 160
+    q = rng.integers(0, 4, size=(n, k), dtype=np.uint8)
+    scale = rng.uniform(1e-3, 2e-2, size=(n, k // 32)).astype(np.float32)
+    w = make_w(2, q, scale, None)
+    assert np.array_equal(oracle.codes(w), q.astype(np.int32))
+    assert np.array_equal(oracle.dequant(w), dense_dequant(2, q, w))
+    xq = rng.integers(-127, 128, size=k).astype(np.int8)
+    ref = (q.reshape(n, k // 32, 32).astype(np.int64) * xq.reshape(k // 32, 32)).sum(2)
+    assert np.array_equal(oracle.blockdots(w, xq), ref)
+    x = rng.standard_normal(k).astype(np.float32)
+    xq2, s, S = oracle.quantize_act(x)
+    assert np.allclose(oracle.gemv(w, x), dense_dequant(2, q, w) @ (np.repeat(s.astype(np.float64), 32) * xq2),
+                       rtol=1e-13, atol=1e-15)
+
+
+def test_q2_zero_point_closed_forms():
+    """All codes 2 decode to zero weights; all codes 3 give y = scale * sum(x_deq)."""
+    k = 96
+    x = datagen.normal_f32(91, 1, k)
+    xq, s, S = oracle.quantize_act(x)
+    assert oracle.gemv(make_w(2, np.full((1, k), 2, np.uint8), 0.5, None), x)[0] == 0.0
+    ref = sum(0.5 * float(s[b]) * int(S[b]) for b in range(k // 32))
+    assert math.isclose(oracle.gemv(make_w(2, np.full((1, k), 3, np.uint8), 0.5, None), x)[0], ref, rel_tol=1e-14)
+
+
+def test_q2_reconstructs_the_drawn_weights():
+    n, k = 16, 256
+    wq = datagen.make_quantized(2, 92, n, k)
+    raw = datagen.weights_f32(92, n, k).astype(np.float64)
+    d = np.repeat(wq["scale"].view(np.float16).astype(np.float64), 32, 1)
+    err = np.abs(oracle.dequant(wq) - raw)
+    assert np.all(err <= 0.5 * d * (1 + 2.0 ** -9) + 1e-12)
+    assert np.max(err / d) > 0.3

@@ -27,6 +27,11 @@
  *      hi     uint8 [n][k/4]: 8 bytes per block, byte 8*b + t holding the top
  *             2 bits of codes 32*b + t, +8, +16, +24 in bits 0-1, 2-3, 4-5, 6-7.
  *  scale, min binary16 (as uint16 bits) [n][k/32]; weight = scale*code + min.
+ *  Q2  codes  uint8 [n][k/4]: 8 bytes per block, byte 8*b + t holding the 2-bit codes
+ *             32*b + t, +8, +16, +24 in bits 0-1, 2-3, 4-5, 6-7; scale binary16
+ *             [n][k/32]; no min plane: weight = scale*(code - 2) (the int2 weights with
+ *             zero point 2 of the Gemma WebGPU Engine, "Roadmap").  Where a call takes
+ *             bits = 2, `lo` is the code plane and `hi` and `min` are NULL.
  *  CQ  idx    uint8 [n][k/2]: index 2j in bits 0-3 of byte j, 2j+1 in bits 4-7;
  *      codebook binary16 [16]; row_scale binary16 [n].
  * Packed planes, x and y must start on 16-byte boundaries.
@@ -94,6 +99,9 @@ int qgemv_q4(const uint8_t* codes, const uint16_t* scale, const uint16_t* min, i
              float* y, unsigned flags, void* stream);
 
 /* qgemv_q6: as qgemv_q4 with 6-bit codes (lo, hi planes). */
+/* qgemv_q2: as qgemv_q4 with 2-bit codes (Q2 layout), w = scale*(code - 2). */
+int qgemv_q2(const uint8_t* codes, const uint16_t* scale, int n, int k, const float* x, float* y, unsigned flags,
+             void* stream);
 int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n, int k,
              const float* x, float* y, unsigned flags, void* stream);
 
@@ -102,7 +110,7 @@ int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const 
  * column X[c] (fp32 [k], contiguous rows of X [batch][k]) is quantised on its
  * own and all columns share one pass over the weights (the multi-token int8
  * kernels of the oxinfer README, "Speculative decoding" and "How it works").
- *   bits : 4 (hi must be NULL) or 6
+ *   bits : 2 (hi and min NULL), 4 (hi NULL) or 6
  *   1 <= batch <= QG_MAX_BATCH;  batch * k <= 131072
  *   X : device fp32 [batch][k];  Y : device fp32 [batch][n] (written)
  * For batch >= 8 with 4-bit weights and k in {512, 1024, 2048, 4096} the integer
@@ -150,7 +158,7 @@ size_t qg_vocab_workspace_bytes(void);
  * as is), and the index of the largest logit, the lowest index among equal
  * maxima and NaN never winning (the deterministic argmax of the Gemma WebGPU
  * Engine, "Roadmap").
- *   bits : 4 or 6;  logits : device fp32 [n_vocab] or NULL (not written);
+ *   bits : 2, 4 or 6 (the pages' LM head is int2);  logits : device fp32 [n_vocab] or NULL;
  *   argmax : device int32 [1] (written);  ws : see qg_vocab_workspace_bytes.
  *   1 <= n_vocab
  */

@@ -35,6 +35,7 @@ SIGNATURES = {
     "qg_device_error": (_i, [ctypes.POINTER(ctypes.c_uint32)]),
     "qgemv_q4": (_i, [_u8p, _u16p, _u16p, _i, _i, _f32p, _f32p, _u, _vp]),
     "qgemv_q6": (_i, [_u8p, _u8p, _u16p, _u16p, _i, _i, _f32p, _f32p, _u, _vp]),
+    "qgemv_q2": (_i, [_u8p, _u16p, _i, _i, _f32p, _f32p, _u, _vp]),
     "qg_batched_workspace_bytes": (_sz, [_i, _i, _i]),
     "qgemv_batched": (_i, [_i, _u8p, _u8p, _u16p, _u16p, _i, _i, _i, _f32p, _f32p, _vp, _sz, _u, _vp]),
     "cq_fwht_matvec": (_i, [_u8p, _u16p, _u16p, _i, _i, _i, _i, _i, _f32p, _f32p, _u, _vp]),
@@ -133,6 +134,25 @@ def qgemv_q4(codes, scale, min, x, y=None, flags: int = 0):
     return y
 
 
+def qgemv_q2(codes, scale, x, y=None, flags: int = 0):
+    """y[n] = GEMV of 2-bit weights (codes [n][k/4] uint8, scale [n][k/32] binary16, w = scale*(code-2)) with x[k]."""
+    _need(codes, "codes", _U8)
+    dev = codes.device
+    _need(scale, "scale", _H16, dev)
+    _need(x, "x", _F32, dev)
+    n, k = codes.shape[0], codes.shape[1] * 4
+    if y is None:
+        y = torch.empty(n, dtype=torch.float32, device=dev)
+    _need(y, "y", _F32, dev)
+    with torch.cuda.device(dev):
+        _check(lib().qgemv_q2(_ptr(codes), _ptr(scale), n, k, _ptr(x), _ptr(y), flags, _stream(dev)), "qgemv_q2")
+    return y
+
+
+def _k_of(bits, lo):
+    return lo.shape[1] * (4 if bits == 2 else 2)
+
+
 def qgemv_q6(lo, hi, scale, min, x, y=None, flags: int = 0):
     """As :func:`qgemv_q4` for 6-bit codes (lo [n][k/2], hi [n][k/4])."""
     _need(lo, "lo", _U8)
@@ -164,10 +184,11 @@ def qgemv_batched(bits, lo, hi, scale, min, X, Y=None, flags: int = 0, ws="auto"
     dev = lo.device
     if bits == 6:
         _need(hi, "hi", _U8, dev)
-    for t, nm in ((scale, "scale"), (min, "min")):
-        _need(t, nm, _H16, dev)
+    _need(scale, "scale", _H16, dev)
+    if bits != 2:
+        _need(min, "min", _H16, dev)
     _need(X, "X", _F32, dev)
-    n, k = lo.shape[0], lo.shape[1] * 2
+    n, k = lo.shape[0], _k_of(bits, lo)
     batch = X.shape[0] if X.dim() == 2 else 1
     if Y is None:
         Y = torch.empty(batch, n, dtype=torch.float32, device=dev)
@@ -177,7 +198,7 @@ def qgemv_batched(bits, lo, hi, scale, min, X, Y=None, flags: int = 0, ws="auto"
     if ws is not None:
         _need(ws, "ws", None, dev)
     with torch.cuda.device(dev):
-        _check(lib().qgemv_batched(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min), n, k,
+        _check(lib().qgemv_batched(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min) if bits != 2 else None, n, k,
                                    batch, _ptr(X), _ptr(Y), _ptr(ws), 0 if ws is None else ws.numel(), flags,
                                    _stream(dev)), "qgemv_batched")
     return Y
@@ -216,10 +237,11 @@ def vocab_softcap_argmax(bits, lo, hi, scale, min, x, softcap: float = 30.0, log
     dev = lo.device
     if bits == 6:
         _need(hi, "hi", _U8, dev)
-    for t, nm in ((scale, "scale"), (min, "min")):
-        _need(t, nm, _H16, dev)
+    _need(scale, "scale", _H16, dev)
+    if bits != 2:
+        _need(min, "min", _H16, dev)
     _need(x, "x", _F32, dev)
-    n, k = lo.shape[0], lo.shape[1] * 2
+    n, k = lo.shape[0], _k_of(bits, lo)
     if logits is True:
         logits = torch.empty(n, dtype=torch.float32, device=dev)
     elif logits is False:
@@ -233,7 +255,7 @@ def vocab_softcap_argmax(bits, lo, hi, scale, min, x, softcap: float = 30.0, log
         ws = vocab_workspace(dev)
     _need(ws, "ws", None, dev)
     with torch.cuda.device(dev):
-        _check(lib().vocab_softcap_argmax(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min), n,
+        _check(lib().vocab_softcap_argmax(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min) if bits != 2 else None, n,
                                           k, _ptr(x), float(softcap), _ptr(logits), _ptr(argmax), _ptr(ws),
                                           ws.numel() * ws.element_size(), flags, _stream(dev)),
                "vocab_softcap_argmax")
@@ -331,18 +353,19 @@ def vocab_softcap_select(bits, lo, hi, scale, min, x, softcap: float = 30.0, all
     dev = lo.device
     if bits == 6:
         _need(hi, "hi", _U8, dev)
-    for t, nm in ((scale, "scale"), (min, "min")):
-        _need(t, nm, _H16, dev)
+    _need(scale, "scale", _H16, dev)
+    if bits != 2:
+        _need(min, "min", _H16, dev)
     _need(x, "x", _F32, dev)
     if allowed is not None:
         _need(allowed, "allowed", (torch.int32,), dev)
-    n, k = lo.shape[0], lo.shape[1] * 2
+    n, k = lo.shape[0], _k_of(bits, lo)
     logits = torch.empty(n, dtype=torch.float32, device=dev) if logits is None else logits
     token = torch.empty(1, dtype=torch.int32, device=dev) if token is None else token
     logprob = torch.empty(1, dtype=torch.float32, device=dev) if logprob is None else logprob
     ws = vocab_select_workspace(dev) if ws is None else ws
     with torch.cuda.device(dev):
-        _check(lib().vocab_softcap_select(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min), n,
+        _check(lib().vocab_softcap_select(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, _ptr(scale), _ptr(min) if bits != 2 else None, n,
                                           k, _ptr(x), float(softcap), _ptr(allowed),
                                           0 if allowed is None else allowed.numel(), _ptr(logits), _ptr(token),
                                           _ptr(logprob), _ptr(ws), ws.numel() * ws.element_size(), flags,
@@ -372,7 +395,7 @@ def qg_blockdots(bits, lo, hi, xq):
     if bits == 6:
         _need(hi, "hi", _U8, dev)
     _need(xq, "xq", (torch.int8,), dev)
-    n, k = lo.shape[0], lo.shape[1] * 2
+    n, k = lo.shape[0], _k_of(bits, lo)
     dots = torch.empty(n, k // 32, dtype=torch.int32, device=dev)
     with torch.cuda.device(dev):
         _check(lib().qg_blockdots(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, n, k, _ptr(xq), _ptr(dots),

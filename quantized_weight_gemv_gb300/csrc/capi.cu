@@ -84,11 +84,13 @@ int ensure_smem_attr(const void* kernel, size_t smem, const LaunchCtx& lc) {
 
 static int check_weights(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
                          int n, int k) {
-    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
     if (n < 0 || k <= 0 || (k & 31) != 0 || k > QG_MAX_K) return QG_ERR_INVALID_ARG;
     if (n == 0) return QG_OK;
-    if (!lo || !scale || !min || (bits == 6 && !hi) || (bits == 4 && hi)) return QG_ERR_INVALID_ARG;
-    if (!aligned16(lo) || (bits == 6 && !aligned16(hi)) || !aligned16(scale) || !aligned16(min))
+    // Q2 has no hi and no min plane (zero point 2); Q4 no hi plane
+    if (!lo || !scale || (bits != 2 && !min) || (bits == 2 && min) || (bits == 6 && !hi) || (bits != 6 && hi))
+        return QG_ERR_INVALID_ARG;
+    if (!aligned16(lo) || (bits == 6 && !aligned16(hi)) || !aligned16(scale) || (bits != 2 && !aligned16(min)))
         return QG_ERR_ALIGNMENT;
     return QG_OK;
 }
@@ -162,6 +164,11 @@ int qg_device_error(uint32_t* code) {
 int qgemv_q4(const uint8_t* codes, const uint16_t* scale, const uint16_t* min, int n, int k, const float* x,
              float* y, unsigned flags, void* stream) {
     return gemv_common(4, codes, nullptr, scale, min, n, k, 1, x, y, nullptr, 0, flags, stream);
+}
+
+int qgemv_q2(const uint8_t* codes, const uint16_t* scale, int n, int k, const float* x, float* y, unsigned flags,
+             void* stream) {
+    return gemv_common(2, codes, nullptr, scale, nullptr, n, k, 1, x, y, nullptr, 0, flags, stream);
 }
 
 int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min, int n, int k,
@@ -303,10 +310,10 @@ int qg_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int
 
 int qg_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,
                  void* stream) {
-    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
     if (n < 0 || k <= 0 || (k & 31) != 0 || k > QG_MAX_K) return QG_ERR_INVALID_ARG;
     if (n == 0) return QG_OK;
-    if (!lo || !xq || !dots || (bits == 6 && !hi) || (bits == 4 && hi)) return QG_ERR_INVALID_ARG;
+    if (!lo || !xq || !dots || (bits == 6 && !hi) || (bits != 6 && hi)) return QG_ERR_INVALID_ARG;
     if (!aligned16(lo) || (bits == 6 && !aligned16(hi)) || !aligned16(xq)) return QG_ERR_ALIGNMENT;
     LaunchCtx lc;
     int rc = resolve(stream, 0, lc);

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
 
     float bv = __int_as_float(0x7fc00000);
     int bi = 0x7fffffff;
-    const size_t code_row = (size_t)(p.k >> 1), hi_row = (size_t)(p.k >> 2);
+    const size_t code_row = (size_t)(BITS == 2 ? p.k >> 2 : p.k >> 1), hi_row = (size_t)(p.k >> 2);
 
     for (int r = blockIdx.x * 8 + wid; r < p.n; r += gridDim.x * 8) {
         float acc[BC];
@@ -35,14 +35,19 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
         const uint8_t* crow = p.lo + (size_t)r * code_row;
         const uint8_t* hrow = (BITS == 6) ? p.hi + (size_t)r * hi_row : nullptr;
         const uint16_t* srow = p.scale + (size_t)r * nb;
-        const uint16_t* mrow = p.min + (size_t)r * nb;
+        const uint16_t* mrow = BITS == 2 ? nullptr : p.min + (size_t)r * nb;  // Q2: zero point 2, no min plane
 #pragma unroll 2
         for (int b = lane; b < nb; b += 32) {
-            const uint4 cw = ldg_stream16(crow + 16 * (size_t)b);
+            uint4 cw = make_uint4(0u, 0u, 0u, 0u);
             uint2 hw = make_uint2(0u, 0u);
-            if constexpr (BITS == 6) hw = ldg_stream8(hrow + 8 * (size_t)b);
+            if constexpr (BITS == 2) {
+                hw = ldg_stream8(crow + 8 * (size_t)b);
+            } else {
+                cw = ldg_stream16(crow + 16 * (size_t)b);
+                if constexpr (BITS == 6) hw = ldg_stream8(hrow + 8 * (size_t)b);
+            }
             const float d = half_bits_to_float(ldg_stream2(srow + b));
-            const float m = half_bits_to_float(ldg_stream2(mrow + b));
+            const float m = BITS == 2 ? -2.0f * d : half_bits_to_float(ldg_stream2(mrow + b));
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
                 if (c < p.batch) {
@@ -109,9 +114,14 @@ __global__ void __launch_bounds__(256) blockdots_kernel(const uint8_t* __restric
          t += (long long)gridDim.x * blockDim.x) {
         const long long r = t / nb;
         const int b = (int)(t - r * nb);
-        const uint4 cw = ldg_stream16(lo + r * (k >> 1) + 16 * b);
+        uint4 cw = make_uint4(0u, 0u, 0u, 0u);
         uint2 hw = make_uint2(0u, 0u);
-        if constexpr (BITS == 6) hw = ldg_stream8(hi + r * (k >> 2) + 8 * b);
+        if constexpr (BITS == 2) {
+            hw = ldg_stream8(lo + r * (k >> 2) + 8 * b);
+        } else {
+            cw = ldg_stream16(lo + r * (k >> 1) + 16 * b);
+            if constexpr (BITS == 6) hw = ldg_stream8(hi + r * (k >> 2) + 8 * b);
+        }
         const uint4 xl = *reinterpret_cast<const uint4*>(xq + 32 * b);
         const uint4 xh = *reinterpret_cast<const uint4*>(xq + 32 * b + 16);
         dots[t] = qdot<BITS>(cw, hw, xl, xh);
@@ -136,10 +146,15 @@ static int launch_plain_t(const PlainParams& p, const LaunchCtx& lc) {
 
 int launch_plain(const PlainParams& p, int bits, int epi, const LaunchCtx& lc) {
     const int bc = p.batch <= 1 ? 1 : p.batch <= 2 ? 2 : p.batch <= 4 ? 4 : p.batch <= 8 ? 8 : 16;
-    if (epi == EPI_ARGMAX) return bits == 4 ? launch_plain_t<4, 1, EPI_ARGMAX>(p, lc) : launch_plain_t<6, 1, EPI_ARGMAX>(p, lc);
-#define QG_CASE(B)                                                                                  \
-    case B:                                                                                         \
-        return bits == 4 ? launch_plain_t<4, B, EPI_STORE>(p, lc) : launch_plain_t<6, B, EPI_STORE>(p, lc);
+    if (epi == EPI_ARGMAX)
+        return bits == 2   ? launch_plain_t<2, 1, EPI_ARGMAX>(p, lc)
+               : bits == 4 ? launch_plain_t<4, 1, EPI_ARGMAX>(p, lc)
+                           : launch_plain_t<6, 1, EPI_ARGMAX>(p, lc);
+#define QG_CASE(B)                                                     \
+    case B:                                                            \
+        return bits == 2   ? launch_plain_t<2, B, EPI_STORE>(p, lc)    \
+               : bits == 4 ? launch_plain_t<4, B, EPI_STORE>(p, lc)    \
+                           : launch_plain_t<6, B, EPI_STORE>(p, lc);
     switch (bc) {
         QG_CASE(1)
         QG_CASE(2)
@@ -163,6 +178,8 @@ int launch_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int 
     const long long total = (long long)n * (k >> 5);
     long long grid = (total + 255) / 256;
     if (grid > lc.sm_count * 16) grid = lc.sm_count * 16;
+    if (bits == 2)
+        return launch_kernel(blockdots_kernel<2>, dim3((unsigned)grid), dim3(256), 0, lc, lo, hi, n, k, xq, dots);
     if (bits == 4)
         return launch_kernel(blockdots_kernel<4>, dim3((unsigned)grid), dim3(256), 0, lc, lo, hi, n, k, xq, dots);
     return launch_kernel(blockdots_kernel<6>, dim3((unsigned)grid), dim3(256), 0, lc, lo, hi, n, k, xq, dots);

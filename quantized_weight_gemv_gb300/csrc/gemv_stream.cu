@@ -4,7 +4,7 @@
 namespace qg {
 
 bool stream_supported(int bits, int n, int k, int batch, int epi) {
-    if (bits != 4 && bits != 6) return false;
+    if (bits != 2 && bits != 4 && bits != 6) return false;
     if (k < 256 || k > 16384 || (k & (k - 1)) != 0) return false;  // nb a power of two in [8, 512]
     if (batch < 1 || batch > 4) return false;
     if (epi == EPI_ARGMAX && batch != 1) return false;
@@ -19,6 +19,7 @@ int launch_stream(const StreamParams& p0, int bits, int epi, const LaunchCtx& lc
     int l = 0;
     while ((1 << l) < nb) ++l;
     p.log2nb = l;
+    if (bits == 2) return launch_stream_bits<2>(p, epi, lc);
     return bits == 4 ? launch_stream_bits<4>(p, epi, lc) : launch_stream_bits<6>(p, epi, lc);
 }
 

@@ -83,13 +83,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Slot layout: codes[256][16] | [hi[256][8]] | scale[256] | min[256]
+// Slot layout: codes[256][CODE] | [hi[256][8]] | scale[256] | [min[256]]
+// (Q4/Q6: 16-byte code blocks; Q2: 8-byte code blocks and no min plane)
 template <int BITS>
 struct Slot {
-    static constexpr int BPB = 16 + (BITS == 6 ? 8 : 0) + 4;
+    static constexpr int CODE = BITS == 2 ? 8 : 16;
+    static constexpr int BPB = CODE + (BITS == 6 ? 8 : 0) + (BITS == 2 ? 2 : 4);
     static constexpr int BYTES = SBW * BPB;
     static constexpr int HI = SBW * 16;
-    static constexpr int SC = SBW * (BITS == 6 ? 24 : 16);
+    static constexpr int SC = SBW * (CODE + (BITS == 6 ? 8 : 0));
     static constexpr int MN = SC + SBW * 2;
 };
 
@@ -187,10 +189,10 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         unsigned char* st = slots + (size_t)(t % D) * SL::BYTES;
         uint64_t* bar = &full[t % D];
         mbar_arrive_expect_tx(bar, blocks * SL::BPB);
-        bulk_g2s(st, p.lo + blk0 * 16, blocks * 16, bar, pol);
+        bulk_g2s(st, p.lo + blk0 * SL::CODE, blocks * SL::CODE, bar, pol);
         if constexpr (BITS == 6) bulk_g2s(st + SL::HI, p.hi + blk0 * 8, blocks * 8, bar, pol);
         bulk_g2s(st + SL::SC, p.scale + blk0, blocks * 2, bar, pol);
-        bulk_g2s(st + SL::MN, p.min + blk0, blocks * 2, bar, pol);
+        if constexpr (BITS != 2) bulk_g2s(st + SL::MN, p.min + blk0, blocks * 2, bar, pol);
     };
 
     if (lane == 0) {
@@ -249,13 +251,19 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
 #pragma unroll
         for (int j = 0; j < JPL; ++j) {
             const int fb = lane + 32 * j;
-            cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
-            if constexpr (BITS == 6)
-                hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
-            else
-                hw[j] = make_uint2(0u, 0u);
+            if constexpr (BITS == 2) {
+                cw[j] = make_uint4(0u, 0u, 0u, 0u);
+                hw[j] = *reinterpret_cast<const uint2*>(st + 8 * fb);
+                mh[j] = 0;
+            } else {
+                cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
+                if constexpr (BITS == 6)
+                    hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+                else
+                    hw[j] = make_uint2(0u, 0u);
+                mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
+            }
             dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
-            mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
         }
         __syncwarp();
         if (lane == 0 && t + D < my_stages) {
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
             const int rloc = (NB >= SBW) ? 0 : ((lane + 32 * j) >> LOG2NB);
 
             const float d = half_bits_to_float(dh[j]);
-            const float m = half_bits_to_float(mh[j]);
+            const float m = BITS == 2 ? -2.0f * d : half_bits_to_float(mh[j]);  // Q2: zero point 2
             const bool valid = rloc < rows_u;
 #pragma unroll
             for (int c = 0; c < BC; ++c) {

@@ -220,10 +220,31 @@ __device__ __forceinline__ int block_dot_q4(uint4 c, uint4 xlo, uint4 xhi) {
     return a + (b >> 4);
 }
 
-// block dot of either format from its raw words (hw unused for Q4)
+// Q2 block dot from its 8 code bytes (word h0 = bytes 0..3, h1 = bytes 4..7; byte t
+// holds codes t, t+8, t+16, t+24 at bit pairs 0..3).  Bit pair s of h0 / h1 meets the
+// activation word 2s / 2s+1 of the block (elements 8s..8s+3 / 8s+4..8s+7), i.e. words
+// of the low half for s < 2 and of the high half for s >= 2.  The pairs are masked in
+// place (4^s * code, at most 192) and dotted as unsigned bytes; the four sums are
+// exact multiples of 4^s.
+__device__ __forceinline__ int block_dot_q2(uint2 c, uint4 xlo, uint4 xhi) {
+    int a0 = __dp4a((int)(c.x & 0x03030303u), (int)xlo.x, 0);
+    a0 = __dp4a((int)(c.y & 0x03030303u), (int)xlo.y, a0);
+    int a1 = dp4a_us(c.x & 0x0C0C0C0Cu, xlo.z, 0);
+    a1 = dp4a_us(c.y & 0x0C0C0C0Cu, xlo.w, a1);
+    int a2 = dp4a_us(c.x & 0x30303030u, xhi.x, 0);
+    a2 = dp4a_us(c.y & 0x30303030u, xhi.y, a2);
+    int a3 = dp4a_us(c.x & 0xC0C0C0C0u, xhi.z, 0);
+    a3 = dp4a_us(c.y & 0xC0C0C0C0u, xhi.w, a3);
+    return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
+}
+
+// block dot of any format from its raw words: Q4 cw; Q6 cw and hw; Q2 hw (8 code bytes)
 template <int BITS>
 __device__ __forceinline__ int qdot(uint4 cw, uint2 hw, uint4 xlo, uint4 xhi) {
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+        (void)cw;
+        return block_dot_q2(hw, xlo, xhi);
+    } else if constexpr (BITS == 4) {
         (void)hw;
         return block_dot_q4(cw, xlo, xhi);
     } else {

@@ -19,7 +19,9 @@ def dev_w(w):
 
 def gpu_gemv(wd, x, flags=0):
     xt = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(DEV)
-    if wd["bits"] == 4:
+    if wd["bits"] == 2:
+        y = qg.qgemv_q2(wd["lo"], wd["scale"], xt, flags=flags)
+    elif wd["bits"] == 4:
         y = qg.qgemv_q4(wd["lo"], wd["scale"], wd["min"], xt, flags=flags)
     else:
         y = qg.qgemv_q6(wd["lo"], wd["hi"], wd["scale"], wd["min"], xt, flags=flags)

@@ -167,3 +167,18 @@ def test_select_validation(lib):
     assert g(6, A16, A16, A16, A16, 8, 64, A16, 30.0, None, 0, None, A16, A16, A16, vws, 0, None) == qg.QG_ERR_INVALID_ARG
     assert g(6, A16, A16, A16, A16, 8, 64, A16, 30.0, None, 0, A16, A16, A16, A16, vws - 1, 0, None) == qg.QG_ERR_WORKSPACE
     assert g(3, A16, A16, A16, A16, 8, 64, A16, 30.0, None, 0, A16, A16, A16, A16, vws, 0, None) == qg.QG_ERR_UNSUPPORTED
+
+
+def test_q2_validation(lib):
+    f = lib.qgemv_q2
+    assert f(A16, A16, 4, 48, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(MIS, A16, 4, 64, A16, A16, 0, None) == qg.QG_ERR_ALIGNMENT
+    assert f(A16, None, 4, 64, A16, A16, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(None, None, 0, 64, None, None, 0, None) == qg.QG_OK
+    b = lib.qgemv_batched
+    assert b(2, A16, None, A16, A16, 4, 64, 1, A16, A16, None, 0, 0, None) == qg.QG_ERR_INVALID_ARG  # min given
+    assert b(2, A16, A16, A16, None, 4, 64, 1, A16, A16, None, 0, 0, None) == qg.QG_ERR_INVALID_ARG  # hi given
+    v = lib.vocab_softcap_argmax
+    ws = lib.qg_vocab_workspace_bytes()
+    assert v(2, A16, None, A16, A16, 8, 64, A16, 30.0, None, A16, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert lib.qgemv_grouped(2, A16, 1, A16, 16, 0, None) == qg.QG_ERR_UNSUPPORTED

@@ -59,11 +59,11 @@ def test_quantize_act_bit_exact(k, batch):
 
 
 # ---------------------------------------------------------------- block dots (bit-exact)
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits", [2, 4, 6])
 @pytest.mark.parametrize("n,k", [(1, 32), (37, 96), (300, 2048)])
 def test_blockdots_bit_exact(bits, n, k):
     rng = np.random.default_rng(n + k + bits)
-    q = rng.integers(0, 16 if bits == 4 else 64, size=(n, k), dtype=np.uint8)
+    q = rng.integers(0, 1 << bits, size=(n, k), dtype=np.uint8)
     w = make_w(bits, q, 1.0, 0.0)
     xq = rng.integers(-127, 128, size=k).astype(np.int8)
     wd = dev_w(w)
@@ -90,7 +90,7 @@ SHAPES = [(1, 32), (7, 96), (33, 256), (100, 512), (1000, 1024), (1024, 1024), (
           (77, 4096), (19, 8192), (40, 16384), (3, 1056), (5, 32768)]
 
 
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits", [2, 4, 6])
 @pytest.mark.parametrize("n,k", SHAPES)
 @pytest.mark.parametrize("flags", FLAGS)
 def test_gemv_random(bits, n, k, flags):
@@ -163,7 +163,7 @@ def test_gemv_empty_is_noop():
 
 
 # ---------------------------------------------------------------- batched
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits", [2, 4, 6])
 @pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 16])
 @pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
 def test_batched(bits, batch, flags):
@@ -212,7 +212,7 @@ def _vocab_check(w, x, softcap, flags=0, ws=None):
     return idx
 
 
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits", [2, 4, 6])
 @pytest.mark.parametrize("n,k", [(1, 32), (1000, 256), (5000, 2048), (3001, 1056), (700, 16384)])
 @pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
 def test_vocab_random(bits, n, k, flags):
@@ -421,3 +421,27 @@ def test_vocab_softcap_select(bits):
             if top2[1] - top2[0] > 2 * TOL * max(abs(top2[1]), float(np.sqrt(np.mean(ref_l ** 2)))):
                 assert int(tok.item()) == ref_tok
             assert abs(float(lp.item()) - ref_lp) <= TOL * max(1.0, abs(ref_lp))
+
+
+# ---------------------------------------------------------------- 2-bit codes, zero point 2
+def test_q2_zero_point_closed_forms():
+    """Codes 2 decode to zero weights (y = 0 exactly); codes 3 give y = scale * sum(x_deq)."""
+    k = 2048
+    x = datagen.normal_f32(95, 1, k)
+    xq, s, S = oracle.quantize_act(x)
+    for code, ref in ((2, 0.0), (3, sum(0.25 * float(s[b]) * int(S[b]) for b in range(k // 32)))):
+        w = make_w(2, np.full((40, k), code, np.uint8), 0.25, None)
+        for flags in (0, qg.QG_FLAG_PLAIN):
+            y = gpu_gemv(dev_w(w), x, flags)
+            if code == 2:
+                assert np.array_equal(y, np.zeros(40))
+            else:
+                assert_close(y, np.full(40, ref))
+
+
+def test_q2_vocab_head_shape():
+    """The pages' int2 LM head shape class: many rows, short k (262144 x 1536 there; 65536 x 2048 here)."""
+    n, k = 65536, 2048
+    w = datagen.make_quantized(2, 96, n, k)
+    x = datagen.normal_f32(96, 1, k)
+    _vocab_check(w, x, 30.0)

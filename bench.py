@@ -32,7 +32,7 @@ METRIC = "effective weight GB/s & GEMV/s at batch 1 (fraction of ~8 TB/s HBM)"
 # full decode-layer stream (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None
 # whenever the kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "grouped": {"kernel": "grouped::grouped_gemv_kernel<4,2>", "bytes_per_launch": 2484.18e6},
+    "grouped": None,
     "percall": None,
 }
 
@@ -223,6 +223,57 @@ def time_graph(g, stream, reps, warm=2):
         e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / reps  # ms
+
+
+def time_eager(fn, stream, reps, warm=3):
+    """Device time per call (ms) of `fn` issued `reps` times on `stream`."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def decode_chain_rows(mats, n_layers, total_bytes, stream, reps):
+    """The decode chain on the same weights: every GEMV reads an earlier one's output
+    (q, k, v <- layer input; o <- q; gate, up <- o; down <- gate; next layer <- down),
+    140 dependent phases for 35 layers.  Both launch modes of qgemv_chain."""
+    import torch
+
+    import quantized_weight_gemv_gb300 as qg
+    from datagen import workloads as W
+
+    device = mats[0]["lo"].device
+    src, stages = W.decode_chain_plan(n_layers)
+    yc = [torch.empty(m["n"], device=device) for m in mats]
+    x0 = torch.from_numpy(W.decode_chain_x()).to(device)
+    xc = [x0 if s < 0 else yc[s] for s in src]
+    out = {"phases": len(stages), "gemvs": len(src)}
+    for name, fl, launches in (("persistent", 0, 1), ("launches", qg.QG_FLAG_CHAIN_LAUNCHES, 2 * len(stages))):
+        ch = qg.ChainGemv(4, mats, xc, yc, stages, flags=fl)
+        try:
+            g = graph_of(ch.run, stream)
+            ms = time_graph(g, stream, reps)
+            how = "CUDA graph"
+            del g
+        except Exception as e:  # a launch kind the graph capture refuses: time the eager calls
+            torch.cuda.synchronize()
+            ms = time_eager(ch.run, stream, reps)
+            how = f"eager ({type(e).__name__})"
+        out[name] = {"us_per_token": ms * 1e3, "GBps": total_bytes / (ms * 1e-3) / 1e9,
+                     "us_per_phase": ms * 1e3 / len(stages), "launches_per_token": launches, "timed_as": how}
+    assert qg.device_error() == 0
+    return out
 
 
 def extra_rows(device):
@@ -476,6 +527,7 @@ def run_ours(args, ws, rank, local):
     other_mode = {"launch": other, "ms_per_step": ms_other, "GBps": total_bytes / (ms_other * 1e-3) / 1e9,
                   "gemv_per_s": n_gemv / (ms_other * 1e-3),
                   "launches_per_step": n_gemv if other == "percall" else 2}
+    chain = decode_chain_rows(mats, n_layers, total_bytes, stream, max(20, args.steps // 4)) if rank == 0 else None
     g.replay()  # leave the timed path's outputs in y for the check below
     torch.cuda.synchronize()
 
@@ -526,6 +578,7 @@ def run_ours(args, ws, rank, local):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "other_launch_mode": other_mode,
+        "decode_chain": chain,
         "clocks": clocks,
         "parity": parity,
         "setup_s": {"generate_and_upload": t_gen},

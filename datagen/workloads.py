@@ -6,6 +6,8 @@ Shapes, distributions and seeds:
 * ``decode_layers`` - 35 layers x 7 Q4 projections of a hidden-2048 / FFN-16384
   decoder (q, k, v, o, gate, up, down as N x K below), each with its own seed
   ``1000 + 7*layer + proj`` and its own x ~ N(0, 1) of length K.
+* ``decode_chain`` - the same weights, each GEMV reading an earlier one's output
+  (``decode_chain_plan``); one external x[2048] ~ N(0, 1).
 * ``vocab_q6``   - Q6 W 262144x2048 (N(0, 0.02)), x[2048] N(0, 1); soft-cap 30; seed 2.
 * ``batched_q4`` - Q4 W 16384x2048 (N(0, 0.02)); X[B][2048] N(0, 1), column b drawn
   from offset b*2048 of the activation stream; seed 3.
@@ -75,6 +77,34 @@ def decode_projection(layer: int, proj: int, rows: slice | None = None):
     w = make_quantized(4, seed, n, k)
     x = normal_f32(seed, STREAM_X, k)
     return w, x
+
+
+def decode_chain_plan(n_layers: int = N_LAYERS):
+    """Wiring of the dependent decode chain over the decode-layer projections.
+
+    GEMV 7*layer + proj is projection ``proj`` of ``layer`` (same weights as
+    ``decode_projection``).  Returns (src, stage_sizes): src[j] is the GEMV whose
+    output GEMV j reads (-1: the external input, ``decode_chain_x``), stage_sizes
+    the GEMVs per stage in order.  Per layer four stages:
+      q, k, v  <- the layer input (layer 0: the external input; then the previous down)
+      o        <- q      (stands for the attention output: 2048 values)
+      gate, up <- o      (stands for the normalised residual stream: 2048 values)
+      down     <- gate   (stands for the gated FFN activation: 16384 values)
+    Attention, norms, residual adds and the gate nonlinearity are not part of the
+    chain; each link is one quantised GEMV on the previous link's fp32 output.
+    """
+    src, stages = [], []
+    for layer in range(n_layers):
+        base = 7 * layer
+        inp = -1 if layer == 0 else base - 1
+        src += [inp, inp, inp, base + 0, base + 3, base + 3, base + 4]
+        stages += [3, 1, 2, 1]
+    return src, stages
+
+
+def decode_chain_x() -> np.ndarray:
+    """External input of the decode chain: x[2048] ~ N(0, 1), the layer-0 q activation."""
+    return normal_f32(decode_seed(0, 0), STREAM_X, HIDDEN)
 
 
 def decode_pass_bytes(n_layers: int = N_LAYERS) -> int:

@@ -62,6 +62,9 @@ enum qg_status {
                                writing any output or touching the workspace.  The caller     \
                                guarantees that no preceding work writes the weights.         */
 #define QG_FLAG_PLAIN 0x2u  /* force the plain-load kernel (128-bit loads, no bulk-copy ring) */
+#define QG_FLAG_CHAIN_LAUNCHES 0x4u /* qgemv_chain: one grouped launch pair per phase, chained by  \
+                                       programmatic dependent launch, instead of one persistent    \
+                                       cooperative launch                                          */
 
 /* Largest supported sizes. */
 #define QG_MAX_K 65536       /* qgemv_q4/q6 and vocab: k <= QG_MAX_K */
@@ -75,9 +78,11 @@ const char* qg_status_string(int status);
 int qg_version(void);
 
 /*
- * Device-side error word.  Kernels that wait on an mbarrier give up after a
- * bounded time and record a nonzero code here instead of hanging.  Reads and
- * clears the word of the current device; synchronises the device.
+ * Device-side error word.  Kernels that wait on an mbarrier or on the other CTAs
+ * give up after a bounded time and record a nonzero code here instead of hanging:
+ * 1 a weight tile never landed, 4 a copy in flight never landed while stopping,
+ * 8 a grid-wide barrier of qgemv_chain ran out.  Reads and clears the word of the
+ * current device; synchronises the device.
  * Returns QG_OK or QG_ERR_CUDA; *code receives the word (0 = no error).
  */
 int qg_device_error(uint32_t* code);
@@ -247,6 +252,42 @@ int qgemv_grouped(int bits, const qg_gemv_desc* descs, int count, void* ws, size
  */
 #define QG_NOALLOC_WS_BYTES (2u << 20)
 int qgemv_grouped_noalloc(int bits, const qg_gemv_desc* descs, int count, unsigned flags, void* stream);
+
+/*
+ * qgemv_chain: dependent GEMVs in decode order.  The `count` descriptors form
+ * `n_phases` phases, phase f being the next phase_sizes[f] of them.  A GEMV may read
+ * (x) any vector written by an earlier phase or present before the call; the GEMVs
+ * of one phase are independent of each other.  Each descriptor computes
+ * y = GEMV(weights, x) exactly as qgemv_q4/qgemv_q6 define it, on x as the earlier
+ * phases left it.  (Gemma WebGPU Engine, "Decode pipeline": a token's projections
+ * run layer after layer, each on what the previous one wrote; genie-ai-runtime, "The
+ * decode arc": the activation is quantised per matmul.)
+ *   bits  : 4 (hi NULL) or 6
+ *   descs : HOST array of `count` descriptors, read during the call only; n >= 0 and
+ *           k a power of two with 1024 <= k <= 16384, as for qgemv_grouped
+ *   phase_sizes : HOST int [n_phases], every entry >= 1, summing to count
+ *   1 <= n_phases <= count <= QG_MAX_GROUP
+ *   Within one phase no output may overlap another output or any input of that
+ *   phase, and the distinct inputs (by x and k) total at most QG_CHAIN_MAX_PHASE_K
+ *   values.  Across phases buffers may be reused freely.
+ *   ws : device workspace of at least qg_chain_workspace_bytes(...) bytes, 16-byte
+ *        aligned; its first QG_CHAIN_CTL_BYTES bytes are zero-filled once after
+ *        allocation and every call that completes leaves them zero.  Calls sharing a
+ *        workspace must not overlap on the GPU.
+ * Default: one cooperative launch, one CTA per SM, that streams every phase's
+ * weights through per-warp bulk-copy rings running ahead across phase boundaries,
+ * with a grid-wide barrier between phases.  It starts after the preceding work on the
+ * stream has finished (QG_FLAG_PDL does not apply to it).  A barrier wait gives up
+ * after 1 s: the kernel then records a code in the device error word and stops; the
+ * outputs are undefined.  With QG_FLAG_CHAIN_LAUNCHES each phase runs as the two
+ * launches of qgemv_grouped instead, phase f+1 chained to phase f by programmatic
+ * dependent launch (QG_FLAG_PDL applies to the first phase).
+ */
+#define QG_CHAIN_CTL_BYTES 256
+#define QG_CHAIN_MAX_PHASE_K 32768
+size_t qg_chain_workspace_bytes(const qg_gemv_desc* descs, int count, const int* phase_sizes, int n_phases);
+int qgemv_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase_sizes, int n_phases, void* ws,
+                size_t ws_bytes, unsigned flags, void* stream);
 
 /*
  * Exposed steps, for exactness checks of the integer parts.

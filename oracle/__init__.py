@@ -178,6 +178,32 @@ def gemv_batched(w: dict, X: np.ndarray) -> np.ndarray:
     return np.stack([gemv(w, X[b]) for b in range(X.shape[0])])
 
 
+def gemv_chain(mats, src, inputs, gemv_fn=None):
+    """Outputs (fp64, one per GEMV) of GEMVs run in order, each on an earlier one's output.
+
+    Decode runs its projections back to back: what one matrix-vector product writes
+    is the vector the next one quantises and reads (genie-ai-runtime, "The decode
+    arc": the activation is quantised per matmul; Gemma WebGPU Engine, "Decode
+    pipeline": layer after layer within one token).  GEMV j reads
+      src[j] >= 0 : the output of GEMV src[j] (src[j] < j), handed over as the fp32
+                    vector a kernel writes, i.e. the fp64 result rounded to fp32;
+      src[j] <  0 : the external fp32 vector inputs[-src[j] - 1].
+    Each GEMV is ``gemv`` above (int8-quantised input, exact block dots, fp64 sum);
+    ``gemv_fn`` may replace it by the same function evaluated over row slices in
+    parallel, for large matrices.
+    """
+    gemv_fn = gemv if gemv_fn is None else gemv_fn
+    outs = []
+    for j, w in enumerate(mats):
+        if src[j] >= 0:
+            assert src[j] < j, "a GEMV reads only the outputs of earlier ones"
+            x = outs[src[j]].astype(np.float32)
+        else:
+            x = np.asarray(inputs[-src[j] - 1], np.float32)
+        outs.append(gemv_fn(w, x))
+    return outs
+
+
 def softcap(z, c: float) -> np.ndarray:
     z = _c(np.atleast_1d(z), np.float64)
     out = np.empty_like(z)

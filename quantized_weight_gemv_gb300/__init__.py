@@ -25,6 +25,9 @@ QG_ERR_CUDA = -5
 
 QG_FLAG_PDL = 0x1
 QG_FLAG_PLAIN = 0x2
+QG_FLAG_CHAIN_LAUNCHES = 0x4
+QG_CHAIN_CTL_BYTES = 256
+QG_CHAIN_MAX_PHASE_K = 32768
 
 # every exported function and its ctypes signature (restype, argtypes)
 _u8p = _u16p = _f32p = _i8p = _i32p = _vp = ctypes.c_void_p
@@ -49,6 +52,8 @@ SIGNATURES = {
     "qg_grouped_workspace_bytes": (_sz, [_vp, _i]),
     "qgemv_grouped": (_i, [_i, _vp, _i, _vp, _sz, _u, _vp]),
     "qgemv_grouped_noalloc": (_i, [_i, _vp, _i, _u, _vp]),
+    "qg_chain_workspace_bytes": (_sz, [_vp, _i, _vp, _i]),
+    "qgemv_chain": (_i, [_i, _vp, _i, _vp, _i, _vp, _sz, _u, _vp]),
     "qg_quantize_act": (_i, [_f32p, _i, _i, _i8p, _f32p, _i32p, _vp]),
     "qg_blockdots": (_i, [_i, _u8p, _u8p, _i, _i, _i8p, _i32p, _vp]),
 }
@@ -316,6 +321,36 @@ class GroupedGemv:
 def qgemv_grouped(bits, mats, xs, ys, flags: int = 0):
     """One-shot :class:`GroupedGemv` call; returns ``ys``."""
     GroupedGemv(bits, mats, xs, ys, flags).run()
+    return ys
+
+
+class ChainGemv(GroupedGemv):
+    """A fixed dependent chain of GEMVs run by :func:`qgemv_chain`.
+
+    As :class:`GroupedGemv`, plus ``phase_sizes``: the GEMVs are taken in order, the
+    next ``phase_sizes[f]`` of them forming phase f; a GEMV's ``xs`` entry may be (a
+    view of) the output tensor of a GEMV in an earlier phase.  The workspace is
+    zero-filled once here; every completed call leaves its control words zero.
+    """
+
+    def __init__(self, bits, mats, xs, ys, phase_sizes, flags: int = 0):
+        super().__init__(bits, mats, xs, ys, flags)
+        self.phase_sizes = (ctypes.c_int * len(phase_sizes))(*[int(v) for v in phase_sizes])
+        self.n_phases = len(phase_sizes)
+        nbytes = int(lib().qg_chain_workspace_bytes(ctypes.cast(self.descs, ctypes.c_void_p), self.count,
+                                                    ctypes.cast(self.phase_sizes, ctypes.c_void_p), self.n_phases))
+        self.ws = torch.zeros(max(nbytes, QG_CHAIN_CTL_BYTES), dtype=torch.uint8, device=self.device)
+
+    def run(self):
+        with torch.cuda.device(self.device):
+            _check(lib().qgemv_chain(self.bits, ctypes.cast(self.descs, ctypes.c_void_p), self.count,
+                                     ctypes.cast(self.phase_sizes, ctypes.c_void_p), self.n_phases, _ptr(self.ws),
+                                     self.ws.numel(), self.flags, _stream(self.device)), "qgemv_chain")
+
+
+def qgemv_chain(bits, mats, xs, ys, phase_sizes, flags: int = 0):
+    """One-shot :class:`ChainGemv` call; returns ``ys``."""
+    ChainGemv(bits, mats, xs, ys, phase_sizes, flags).run()
     return ys
 
 

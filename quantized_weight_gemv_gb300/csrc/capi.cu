@@ -271,6 +271,89 @@ size_t qg_grouped_workspace_bytes(const qg_gemv_desc* descs, int count) {
     return grouped_workspace_bytes(descs, count);
 }
 
+// [a, a + na) and [b, b + nb) share a byte
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
+// Shape of a chain: phase sizes, every descriptor as qgemv_grouped wants it, and the
+// per-phase rules (no output overlapping an output or input of its phase; distinct
+// inputs of a phase within QG_CHAIN_MAX_PHASE_K values).
+static int check_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase_sizes, int n_phases,
+                       int* active) {
+    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
+    if (count < 0 || count > QG_MAX_GROUP || n_phases < 0 || n_phases > count) return QG_ERR_INVALID_ARG;
+    *active = 0;
+    if (count == 0) return n_phases == 0 ? QG_OK : QG_ERR_INVALID_ARG;
+    if (!descs || !phase_sizes || n_phases < 1) return QG_ERR_INVALID_ARG;
+    long long sum = 0;
+    for (int f = 0; f < n_phases; ++f) {
+        if (phase_sizes[f] < 1) return QG_ERR_INVALID_ARG;
+        sum += phase_sizes[f];
+    }
+    if (sum != count) return QG_ERR_INVALID_ARG;
+    int off = 0;
+    for (int f = 0; f < n_phases; ++f) {
+        const qg_gemv_desc* ph = descs + off;
+        const int m = phase_sizes[f];
+        long long in_k = 0;
+        for (int i = 0; i < m; ++i) {
+            const qg_gemv_desc& d = ph[i];
+            if (d.n < 0) return QG_ERR_INVALID_ARG;
+            if (d.k < 1024 || d.k > 16384 || (d.k & (d.k - 1)) != 0) return QG_ERR_UNSUPPORTED;
+            if (d.n == 0) continue;
+            int rc = check_weights(bits, d.lo, d.hi, d.scale, d.min, d.n, d.k);
+            if (rc != QG_OK) return rc;
+            if (!d.x || !d.y) return QG_ERR_INVALID_ARG;
+            if (!aligned16(d.x) || !aligned16(d.y)) return QG_ERR_ALIGNMENT;
+            bool seen = false;
+            for (int j = 0; j < i && !seen; ++j) seen = ph[j].n > 0 && ph[j].x == d.x && ph[j].k == d.k;
+            if (!seen) in_k += d.k;
+            ++*active;
+        }
+        if (in_k > QG_CHAIN_MAX_PHASE_K) return QG_ERR_UNSUPPORTED;
+        for (int i = 0; i < m; ++i) {
+            if (ph[i].n == 0) continue;
+            const size_t yb = (size_t)ph[i].n * 4;
+            for (int j = 0; j < m; ++j) {
+                if (ph[j].n == 0) continue;
+                if (overlaps(ph[i].y, yb, ph[j].x, (size_t)ph[j].k * 4)) return QG_ERR_INVALID_ARG;
+                if (j != i && overlaps(ph[i].y, yb, ph[j].y, (size_t)ph[j].n * 4)) return QG_ERR_INVALID_ARG;
+            }
+        }
+        off += m;
+    }
+    return QG_OK;
+}
+
+size_t qg_chain_workspace_bytes(const qg_gemv_desc* descs, int count, const int* phase_sizes, int n_phases) {
+    // 0 for a malformed phase list; descriptors with k out of range add nothing
+    if (!descs || !phase_sizes || count <= 0 || count > QG_MAX_GROUP || n_phases < 1 || n_phases > count) return 0;
+    long long sum = 0;
+    for (int f = 0; f < n_phases; ++f) {
+        if (phase_sizes[f] < 1) return 0;
+        sum += phase_sizes[f];
+    }
+    if (sum != count) return 0;
+    for (int i = 0; i < count; ++i)
+        if (descs[i].k < 1024 || descs[i].k > 16384) return QG_CHAIN_CTL_BYTES;  // the call will refuse it
+    return chain_workspace_bytes(descs, count, phase_sizes, n_phases);
+}
+
+int qgemv_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase_sizes, int n_phases, void* ws,
+                size_t ws_bytes, unsigned flags, void* stream) {
+    int active = 0;
+    int rc = check_chain(bits, descs, count, phase_sizes, n_phases, &active);
+    if (rc != QG_OK || active == 0) return rc;
+    if (!ws || ws_bytes < chain_workspace_bytes(descs, count, phase_sizes, n_phases)) return QG_ERR_WORKSPACE;
+    if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    rc = resolve(stream, flags, lc);
+    if (rc != QG_OK) return rc;
+    return launch_chain(bits, descs, count, phase_sizes, n_phases, reinterpret_cast<unsigned char*>(ws), lc);
+}
+
 int qgemv_grouped(int bits, const qg_gemv_desc* descs, int count, void* ws, size_t ws_bytes, unsigned flags,
                   void* stream) {
     if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;

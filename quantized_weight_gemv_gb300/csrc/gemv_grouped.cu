@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
 
     for (int t = 0; cc.g < u_end; ++t) {
         const int slot = t % D;
-        if (!stream::mbar_wait(&full[slot], (uint32_t)((t / D) & 1))) {
+        if (!__all_sync(0xffffffffu, stream::mbar_wait(&full[slot], (uint32_t)((t / D) & 1)))) {  // warp-uniform
             atomicOr(p.err, ERR_WAIT_FULL);
             break;
         }

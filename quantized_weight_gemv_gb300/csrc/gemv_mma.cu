@@ -129,6 +129,7 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
         }
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
+            if (r0 + i * nthreads >= total) break;  // the same for every thread
             const int idx_all = r0 + i * nthreads + t;
             const int c = idx_all / nf4;
             const int idx = idx_all - c * nf4;
@@ -140,10 +141,11 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
             const float s = __fdiv_rn(a, 127.0f);
             int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
             if (s != 0.0f) {
-                q0 = max(-127, min(127, __float2int_rn(__fdiv_rn(r.x, s))));
-                q1 = max(-127, min(127, __float2int_rn(__fdiv_rn(r.y, s))));
-                q2 = max(-127, min(127, __float2int_rn(__fdiv_rn(r.z, s))));
-                q3 = max(-127, min(127, __float2int_rn(__fdiv_rn(r.w, s))));
+                const float inv = __frcp_rn(s);
+                q0 = quant_code(r.x, s, inv);
+                q1 = quant_code(r.y, s, inv);
+                q2 = quant_code(r.z, s, inv);
+                q3 = quant_code(r.w, s, inv);
             }
             int S = q0 + q1 + q2 + q3;
             S += __shfl_xor_sync(0xffffffffu, S, 1);

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
 
     for (int t = 0; t < my_stages; ++t) {
         const int slot = t % D;
-        if (!mbar_wait(&full[slot], (uint32_t)((t / D) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (uint32_t)((t / D) & 1)))) {  // warp-uniform
             atomicOr(p.err, ERR_WAIT_FULL);
             break;
         }

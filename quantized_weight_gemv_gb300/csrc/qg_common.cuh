@@ -11,7 +11,7 @@ namespace qg {
 
 // Codes OR-ed into the device error word (its address is a kernel parameter) by a
 // kernel whose bounded wait ran out.  Host side: qg_device_error() reads and clears it.
-enum : unsigned { ERR_WAIT_FULL = 1u, ERR_WAIT_EMPTY = 2u, ERR_WAIT_DRAIN = 4u };
+enum : unsigned { ERR_WAIT_FULL = 1u, ERR_WAIT_EMPTY = 2u, ERR_WAIT_DRAIN = 4u, ERR_WAIT_GRID = 8u };
 
 constexpr int WARP = 32;
 // 1 s: far beyond any legitimate wait of these kernels, short enough to keep the context alive.
@@ -54,16 +54,30 @@ __device__ __forceinline__ float half_bits_to_float(unsigned short b) {
 // One block of 32 values held one per lane: s = max|x| / 127 (IEEE fp32 division),
 // q = clamp(round-half-even(x / s), -127, 127), q = 0 when s == 0.  Returns q; s and
 // the block sum S are returned through references (valid in every lane).
+// clamp(round-half-even(fl32(x / s)), -127, 127) for s > 0, the quotient correctly
+// rounded as an fp32 division gives it.  inv = 1/s correctly rounded: t = x * inv is
+// then within 2^-23 |x/s| <= 1.6e-5 of x/s, and fl32(x/s) within 2^-24 |x/s|, so the
+// two can round to different integers only when t lies within ~2.3e-5 of a
+// half-integer.  Outside 1/4096 of one, rint(t) is the answer; inside (and for a NaN
+// or infinite t) the exact quotient decides.
+__device__ __forceinline__ int quant_code(float x, float s, float inv) {
+    const float t = x * inv;
+    const float a = fabsf(t);
+    int q;
+    if (fabsf(a - floorf(a) - 0.5f) > (1.0f / 4096.0f))
+        q = __float2int_rn(t);
+    else
+        q = __float2int_rn(__fdiv_rn(x, s));
+    return max(-127, min(127, q));
+}
+
 __device__ __forceinline__ int quantize_lane(float x, float& s, int& S) {
     float a = fabsf(x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     s = __fdiv_rn(a, 127.0f);
     int q = 0;
-    if (s != 0.0f) {
-        q = __float2int_rn(__fdiv_rn(x, s));
-        q = max(-127, min(127, q));
-    }
+    if (s != 0.0f) q = quant_code(x, s, __frcp_rn(s));
     int t = q;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
@@ -98,7 +112,9 @@ __host__ __device__ constexpr int xq_bytes(int nb) { return 40 * nb; }
 // so eight consecutive lanes hold one block of 32 of one column and a block's max
 // and sum need three shuffles.  All CHUNK loads of a round are issued before any is
 // used, so the prologue costs about one L2 round trip per CHUNK*NT float4s.
-template <int NT>
+// L2ONLY reads x with ld.global.cg: for a vector other SMs wrote during the same
+// launch, which the non-coherent (and L1) path may hold stale.
+template <int NT, bool L2ONLY = false>
 __device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int k, int batch, unsigned char* base,
                                                 int stride, int t) {
     constexpr int CHUNK = 8;
@@ -112,10 +128,11 @@ __device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
             const int idx = r0 + i * NT + t;
-            r[i] = idx < total ? __ldg(x4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[i] = idx < total ? (L2ONLY ? __ldcg(x4 + idx) : __ldg(x4 + idx)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
+            if (r0 + i * NT >= total) break;  // the same for every thread: nothing left in this round
             const int idx = r0 + i * NT + t;
             float a = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
@@ -124,10 +141,11 @@ __device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int
             const float s = __fdiv_rn(a, 127.0f);
             int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
             if (s != 0.0f) {
-                q0 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].x, s))));
-                q1 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].y, s))));
-                q2 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].z, s))));
-                q3 = max(-127, min(127, __float2int_rn(__fdiv_rn(r[i].w, s))));
+                const float inv = __frcp_rn(s);
+                q0 = quant_code(r[i].x, s, inv);
+                q1 = quant_code(r[i].y, s, inv);
+                q2 = quant_code(r[i].z, s, inv);
+                q3 = quant_code(r[i].w, s, inv);
             }
             int S = q0 + q1 + q2 + q3;
             S += __shfl_xor_sync(0xffffffffu, S, 1);

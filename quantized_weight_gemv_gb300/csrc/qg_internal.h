@@ -98,6 +98,10 @@ size_t mma_workspace_bytes(int k, int batch);
 int launch_mma(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc);
 size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count);
 int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc);
+size_t chain_workspace_bytes(const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase);
+// ws: the caller's chain workspace (control words first); arguments already validated
+int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase,
+                 unsigned char* ws, const LaunchCtx& lc);
 int launch_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token, float* logprob,
                   SelectWorkspace* ws, const LaunchCtx& lc);
 int launch_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, const LaunchCtx& lc);

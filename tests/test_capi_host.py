@@ -182,3 +182,63 @@ def test_q2_validation(lib):
     ws = lib.qg_vocab_workspace_bytes()
     assert v(2, A16, None, A16, A16, 8, 64, A16, 30.0, None, A16, A16, ws, 0, None) == qg.QG_ERR_INVALID_ARG
     assert lib.qgemv_grouped(2, A16, 1, A16, 16, 0, None) == qg.QG_ERR_UNSUPPORTED
+
+
+def _chain_args(descs, sizes):
+    D = qg.GemvDesc
+    arr = (D * len(descs))(*descs)
+    ps = (ctypes.c_int * len(sizes))(*sizes)
+    return arr, ctypes.cast(arr, ctypes.c_void_p), ps, ctypes.cast(ps, ctypes.c_void_p)
+
+
+def test_chain_validation(lib):
+    D = qg.GemvDesc
+    W = 0x10000  # weights stand-in
+    X, Y1, Y2 = 0x100000, 0x200000, 0x300000
+    d0 = D(W, None, W, W, X, Y1, 2048, 2048)        # phase 0 reads X
+    d1 = D(W, None, W, W, Y1, Y2, 2048, 2048)       # phase 1 reads phase 0's output
+    keep, vp, ps_keep, ps = _chain_args([d0, d1], [1, 1])
+    need = lib.qg_chain_workspace_bytes(vp, 2, ps, 2)
+    assert need == qg.QG_CHAIN_CTL_BYTES + 40 * 64    # control words + the largest phase's activation image
+    f = lib.qgemv_chain
+    assert f(5, vp, 2, ps, 2, A16, need, 0, None) == qg.QG_ERR_UNSUPPORTED
+    assert f(4, vp, 0, None, 0, None, 0, 0, None) == qg.QG_OK
+    assert f(4, vp, 2, None, 2, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(4, vp, 2, ps, 0, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(4, vp, 2, ps, 3, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG     # more phases than GEMVs
+    assert f(4, vp, 2, None, 2, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
+    assert f(4, vp, 2, ps, 2, None, need, 0, None) == qg.QG_ERR_WORKSPACE
+    assert f(4, vp, 2, ps, 2, A16, need - 1, 0, None) == qg.QG_ERR_WORKSPACE
+    assert f(4, vp, 2, ps, 2, MIS, need, 0, None) == qg.QG_ERR_ALIGNMENT
+    # phase sizes must be >= 1 and sum to count
+    for sizes in ([2, 0], [1, 2], [0, 2]):
+        _, _, pk, p2 = _chain_args([d0, d1], sizes)
+        assert f(4, vp, 2, p2, 2, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG, sizes
+        assert lib.qg_chain_workspace_bytes(vp, 2, p2, 2) == 0
+    # within one phase an output may not overlap an input or another output ...
+    _, vp1, _, ps1 = _chain_args([d0, d1], [2])
+    assert f(4, vp1, 2, ps1, 1, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG   # d1 reads d0's output
+    inplace = D(W, None, W, W, X, X + 1024, 2048, 2048)  # y starts inside x
+    _, vp2, _, ps2 = _chain_args([inplace], [1])
+    assert f(4, vp2, 1, ps2, 1, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG
+    two = [D(W, None, W, W, X, Y1, 2048, 2048), D(W, None, W, W, X, Y1 + 4096, 2048, 2048)]
+    _, vp3, _, ps3 = _chain_args(two, [2])
+    assert f(4, vp3, 2, ps3, 1, A16, need, 0, None) == qg.QG_ERR_INVALID_ARG   # outputs overlap
+    # ... and the distinct inputs of a phase hold at most QG_CHAIN_MAX_PHASE_K values
+    wide = [D(W, None, W, W, X + i * 0x20000, Y1 + i * 0x1000, 8, 16384) for i in range(3)]
+    _, vp4, _, ps4 = _chain_args(wide, [3])
+    big = lib.qg_chain_workspace_bytes(vp4, 3, ps4, 1)
+    assert f(4, vp4, 3, ps4, 1, A16, big, 0, None) == qg.QG_ERR_UNSUPPORTED
+    shared = [D(W, None, W, W, X, Y1 + i * 0x1000, 8, 16384) for i in range(3)]  # one input, three GEMVs
+    _, vp5, _, ps5 = _chain_args(shared, [3])
+    assert lib.qg_chain_workspace_bytes(vp5, 3, ps5, 1) == qg.QG_CHAIN_CTL_BYTES + 3 * 40 * 512
+    # descriptor rules as for qgemv_grouped
+    for bad, rc in ((D(W, None, W, W, X, Y1, 8, 1536), qg.QG_ERR_UNSUPPORTED),
+                    (D(W, None, W, W, X + 4, Y1, 8, 2048), qg.QG_ERR_ALIGNMENT),
+                    (D(W, W, W, W, X, Y1, 8, 2048), qg.QG_ERR_INVALID_ARG),
+                    (D(W, None, W, W, None, Y1, 8, 2048), qg.QG_ERR_INVALID_ARG)):
+        _, vpb, _, psb = _chain_args([bad], [1])
+        assert f(4, vpb, 1, psb, 1, A16, need, 0, None) == rc
+    empty = D(None, None, None, None, None, None, 0, 2048)
+    _, vpe, _, pse = _chain_args([empty, empty], [1, 1])
+    assert f(4, vpe, 2, pse, 2, None, 0, 0, None) == qg.QG_OK

@@ -1,0 +1,212 @@
+"""GPU parity of the dependent GEMV chain (qgemv_chain) against the oracle's chain.
+
+Both launch modes are covered: the persistent cooperative kernel (default) and one
+grouped launch pair per phase (QG_FLAG_CHAIN_LAUNCHES)."""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+import quantized_weight_gemv_gb300 as qg
+from datagen import workloads as W
+from tests._gpu import DEV, assert_close, dev_w, oracle_gemv_par
+
+pytestmark = pytest.mark.gpu
+MODES = [0, qg.QG_FLAG_CHAIN_LAUNCHES]
+
+
+def _oracle_fn(w, x):
+    return oracle_gemv_par(w, x) if w["n"] * w["k"] >= (1 << 22) else oracle.gemv(w, x)
+
+
+def _run_spec(bits, spec, phase_sizes, ext, flags, seed):
+    """spec: [(n, k, src)], src < 0 -> external input -src-1.  Returns (numpy weights,
+    device outputs, chain object)."""
+    ws_np, mats, xs, ys = [], [], [], []
+    ext_t = [torch.from_numpy(e).to(DEV) for e in ext]
+    for i, (n, k, src) in enumerate(spec):
+        w = datagen.make_quantized(bits, seed + i, n, k)
+        ws_np.append(w)
+        mats.append(dev_w(w))
+        ys.append(torch.full((n,), float("nan"), device=DEV))
+    for i, (n, k, src) in enumerate(spec):
+        xs.append(ext_t[-src - 1] if src < 0 else ys[src])
+        assert xs[-1].numel() == k
+    ch = qg.ChainGemv(bits, mats, xs, ys, phase_sizes, flags=flags)
+    ch.run()
+    return ws_np, ys, ch
+
+
+SMALL = [  # (n, k, src); phases [3, 2, 1, 3]
+    (2048, 1024, -1), (1000, 1024, -1), (4096, 2048, -2),
+    (1024, 2048, 0), (7, 4096, 2),
+    (16384, 1024, 3),
+    (300, 16384, 5), (1, 1024, 3), (513, 8192, -3),
+]
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("flags", MODES)
+def test_chain_small(bits, flags):
+    ext = [datagen.normal_f32(40, 1, 1024), datagen.normal_f32(41, 1, 2048), datagen.normal_f32(42, 1, 8192)]
+    ws_np, ys, _ = _run_spec(bits, SMALL, [3, 2, 1, 3], ext, flags, 300)
+    refs = oracle.gemv_chain(ws_np, [s for _, _, s in SMALL], ext, _oracle_fn)
+    for y, r in zip(ys, refs):
+        assert_close(y.cpu().numpy().astype(np.float64), r)
+
+
+@pytest.mark.parametrize("flags", MODES)
+def test_chain_buffer_reuse_and_repeat(flags):
+    """Ping-pong buffers: phase f writes the vector phase f-1 read.  Repeated calls on one
+    workspace give identical results and leave its control words zero."""
+    n = 2048
+    A = torch.full((n,), float("nan"), device=DEV)
+    B = torch.full((n,), float("nan"), device=DEV)
+    x0 = datagen.normal_f32(50, 1, n)
+    X = torch.from_numpy(x0).to(DEV)
+    ws_np = [datagen.make_quantized(4, 600 + i, n, n) for i in range(6)]
+    mats = [dev_w(w) for w in ws_np]
+    xs = [X, A, B, A, B, A]
+    ys = [A, B, A, B, A, B]
+    ch = qg.ChainGemv(4, mats, xs, ys, [1] * 6, flags=flags)
+    refs = oracle.gemv_chain(ws_np, [-1, 0, 1, 2, 3, 4], [x0])
+    prev = None
+    for rep in range(3):
+        A.fill_(float("nan"))
+        B.fill_(float("nan"))
+        ch.run()
+        torch.cuda.synchronize()
+        a, b = A.cpu().numpy(), B.cpu().numpy()
+        assert_close(a.astype(np.float64), refs[4])
+        assert_close(b.astype(np.float64), refs[5])
+        if prev is not None:
+            assert np.array_equal(a, prev[0]) and np.array_equal(b, prev[1])
+        prev = (a, b)
+        assert int(ch.ws[:qg.QG_CHAIN_CTL_BYTES].count_nonzero()) == 0
+    assert qg.device_error() == 0
+
+
+def test_chain_one_phase_equals_grouped():
+    shapes = [(2048, 2048), (1024, 2048), (16384, 2048), (2048, 16384), (33, 1024)]
+    mats, xs, ys, yg = [], [], [], []
+    for i, (n, k) in enumerate(shapes):
+        mats.append(dev_w(datagen.make_quantized(4, 700 + i, n, k)))
+        xs.append(torch.from_numpy(datagen.normal_f32(700 + i, 1, k)).to(DEV))
+        ys.append(torch.empty(n, device=DEV))
+        yg.append(torch.empty(n, device=DEV))
+    qg.ChainGemv(4, mats, xs, ys, [len(shapes)]).run()
+    qg.qgemv_grouped(4, mats, xs, yg)
+    for a, b in zip(ys, yg):
+        assert torch.equal(a, b)
+
+
+@pytest.fixture(scope="module")
+def decode_chain():
+    """The 35-layer decode chain's weights (numpy and device) and the oracle's outputs."""
+    src, stages = W.decode_chain_plan(W.N_LAYERS)
+    ws_np = [W.decode_projection(j // 7, j % 7)[0] for j in range(len(src))]
+    mats = [dev_w(w) for w in ws_np]
+    x0 = W.decode_chain_x()
+    refs = oracle.gemv_chain(ws_np, src, [x0], _oracle_fn)
+    return src, stages, mats, x0, refs
+
+
+def _decode_run(dc, flags, x0=None):
+    src, stages, mats, x_ref, _ = dc
+    X = torch.from_numpy(x_ref if x0 is None else x0).to(DEV)
+    ys = [torch.full((W.PROJ_SHAPES[j % 7][0],), float("nan"), device=DEV) for j in range(len(src))]
+    xs = [X if s < 0 else ys[s] for s in src]
+    ch = qg.ChainGemv(4, mats, xs, ys, stages, flags=flags)
+    ch.run()
+    return ch, ys, X
+
+
+def _near_tie(x, s, i):
+    """Margin of element i from a rounding boundary of the int8 quantiser, in steps."""
+    t = abs(float(np.float32(x[i]) / np.float32(s[i // 32])))
+    return abs(t - np.floor(t) - 0.5)
+
+
+@pytest.mark.parametrize("flags", MODES)
+def test_decode_chain_full_size(decode_chain, flags):
+    """The 35-layer decode chain (245 GEMVs, 140 phases, 2.48 GB), every output of every GEMV.
+
+    A chain of quantised GEMVs is defined up to the int8 decisions of its hand-offs:
+    fp32 sums of a different order can move a block maximum or an element by an ulp,
+    and an element sitting on a rounding boundary (x/s = 94.5 exactly happens) then
+    rounds the other way - both decisions are correct, and from there on the two chains
+    quantise different vectors and part ways.  So:
+      1. up to the first link whose int8 input codes differ from the oracle's, every
+         output matches the oracle's chain within 1e-3;
+      2. at that link every differing code is off by one at a near-tie of the oracle's
+         own quantisation (a valid alternative decision, not a wrong value);
+      3. every link's output is the verified single-GEMV kernel's result on the vector
+         the link read (fp32 reassociation level), i.e. each link read the finished
+         output of the right earlier link and used the right weights."""
+    src, _, mats, x0, refs = decode_chain
+    _, ys, X = _decode_run(decode_chain, flags)
+    torch.cuda.synchronize()
+    checked = 0
+    for j in range(len(src)):
+        x_dev = X if src[j] < 0 else ys[src[j]]
+        x_or = x0 if src[j] < 0 else refs[src[j]].astype(np.float32)
+        gq = qg.qg_quantize_act(x_dev)[0].cpu().numpy().ravel()
+        oq, os_, _ = oracle.quantize_act(x_or)
+        diff = np.where(gq != oq)[0]
+        if diff.size:
+            for i in diff:
+                assert abs(int(gq[i]) - int(oq[i])) == 1, (j, i)
+                assert _near_tie(x_or, os_, i) < 1e-3, (j, i, _near_tie(x_or, os_, i))
+            break
+        assert_close(ys[j].cpu().numpy().astype(np.float64), refs[j])
+        checked += 1
+    assert checked >= 14, f"only {checked} links before the first tie"  # at least two whole layers
+    for j in range(len(src)):
+        m = mats[j]
+        x_dev = X if src[j] < 0 else ys[src[j]]
+        single = qg.qgemv_q4(m["lo"], m["scale"], m["min"], x_dev)
+        e = oracle.normwise_error(ys[j].cpu().numpy(), single.cpu().numpy())
+        assert e < 1e-5, (j, e)
+    assert qg.device_error() == 0
+
+
+def test_decode_chain_modes_identical_and_equivariant(decode_chain):
+    """Both launch modes give the same bits; scaling the input by 4 scales every output
+    by exactly 4, and negating it negates every output (the activation quantisation is
+    per-block scale-invariant, exact under powers of two and under sign)."""
+    x0 = decode_chain[3]
+    ch, ys, X = _decode_run(decode_chain, 0)
+    base = [y.clone() for y in ys]
+    _, ys2, _ = _decode_run(decode_chain, qg.QG_FLAG_CHAIN_LAUNCHES)
+    for a, b in zip(base, ys2):
+        assert torch.equal(a, b)
+    for factor in (4.0, -1.0):
+        X.copy_(torch.from_numpy(x0 * np.float32(factor)))
+        ch.run()
+        for a, b in zip(base, ys):
+            assert torch.equal(b, a * factor)
+    assert torch.isfinite(base[-1]).all()
+
+
+def test_chain_abort_word_stops_and_rearms():
+    """A set abort word makes every CTA stop at its next phase boundary without waiting
+    out the barrier; the workspace comes back zero and the next call is correct."""
+    n = 2048
+    ws_np = [datagen.make_quantized(4, 800 + i, n, n) for i in range(4)]
+    mats = [dev_w(w) for w in ws_np]
+    x0 = datagen.normal_f32(80, 1, n)
+    X = torch.from_numpy(x0).to(DEV)
+    ys = [torch.empty(n, device=DEV) for _ in range(4)]
+    ch = qg.ChainGemv(4, mats, [X, ys[0], ys[1], ys[2]], ys, [1, 1, 1, 1])
+    ctl = ch.ws[:qg.QG_CHAIN_CTL_BYTES].view(torch.int32)
+    ctl[1] = 1
+    torch.cuda.synchronize()
+    ch.run()
+    torch.cuda.synchronize()
+    assert int(ch.ws[:qg.QG_CHAIN_CTL_BYTES].count_nonzero()) == 0
+    assert qg.device_error() == 0
+    ch.run()
+    refs = oracle.gemv_chain(ws_np, [-1, 0, 1, 2], [x0])
+    for y, r in zip(ys, refs):
+        assert_close(y.cpu().numpy().astype(np.float64), r)

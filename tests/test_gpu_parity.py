@@ -445,3 +445,77 @@ def test_q2_vocab_head_shape():
     w = datagen.make_quantized(2, 96, n, k)
     x = datagen.normal_f32(96, 1, k)
     _vocab_check(w, x, 30.0)
+
+
+# ---------------------------------------------------------------- int8 decisions at ties
+def _tie_x(k, seed):
+    """Activations sitting on the quantiser's rounding boundaries: in every block one
+    element is the maximum 127*c (so s = fl32(127c / 127)), the others fl32((j + 1/2) s)
+    for random j, so x/s is a half-integer or within an ulp of one."""
+    rng = np.random.default_rng(seed)
+    nb = k // 32
+    x = np.empty((nb, 32), np.float32)
+    for b in range(nb):
+        c = np.float32(rng.uniform(0.5, 2.0) * 2.0 ** rng.integers(-12, 12))
+        amax = np.float32(np.float32(127.0) * c)
+        s = np.float32(amax / np.float32(127.0))
+        j = rng.integers(-127, 127, size=32).astype(np.float64)
+        x[b] = (np.float32(1.0) * ((j + 0.5) * np.float64(s))).astype(np.float32)
+        x[b, rng.integers(0, 32)] = amax * np.float32(rng.choice([-1.0, 1.0]))
+    return x.ravel()
+
+
+def _picker(n, k, col):
+    """Q4 weights with scale 1, min 0 and code 1 at (r, col[r]), 0 elsewhere: row r of
+    the GEMV is then s_b * xq[col[r]] exactly, the kernel's own int8 decision."""
+    q = np.zeros((n, k), np.uint8)
+    q[np.arange(n), col] = 1
+    return make_w(4, q, np.ones((n, k // 32)), np.zeros((n, k // 32)))
+
+
+def _expect_picked(x, col):
+    xq, s, _ = oracle.quantize_act(x)
+    return (s[col // 32].astype(np.float32) * xq[col].astype(np.float32)).astype(np.float32)
+
+
+def test_quantize_act_ties_bit_exact():
+    for k, seed in ((1024, 1), (16384, 2)):
+        x = _tie_x(k, seed)
+        xq, xs, xsum = qg.qg_quantize_act(torch.from_numpy(x).to(DEV))
+        oq, os_, oS = oracle.quantize_act(x)
+        assert np.array_equal(xq[0].cpu().numpy(), oq)
+        assert np.array_equal(xs[0].cpu().numpy().view(np.uint32), os_.view(np.uint32))
+        assert np.array_equal(xsum[0].cpu().numpy(), oS)
+        # the inputs really sit on boundaries: many exact ties
+        t = np.abs(x / np.repeat(os_, 32))
+        assert np.sum(np.abs(t - np.floor(t) - 0.5) == 0) > k // 8
+
+
+@pytest.mark.parametrize("k", [1024, 2048, 16384])
+def test_int8_decisions_every_kernel(k):
+    """Every kernel that quantises activations takes the oracle's int8 decisions on tie
+    inputs: single-vector stream and plain kernels, the grouped and chain GEMVs, and the
+    batched dp4a and tensor-core kernels."""
+    n = 2048
+    r = np.arange(n)
+    col = r % k if k <= n else r * (k // n) + r % (k // n)  # every column, or spread over all positions
+    w = dev_w(_picker(n, k, col))
+    X = np.stack([_tie_x(k, 10 + b) for b in range(8)])
+    Xt = torch.from_numpy(X).to(DEV)
+    want = [_expect_picked(X[b], col) for b in range(8)]
+    got = {}
+    for flags in (0, qg.QG_FLAG_PLAIN):
+        got[f"q4 flags={flags}"] = [qg.qgemv_q4(w["lo"], w["scale"], w["min"], Xt[0], flags=flags)]
+    y = torch.empty(n, device=DEV)
+    qg.qgemv_grouped(4, [w], [Xt[0]], [y])
+    got["grouped"] = [y]
+    yc = [torch.empty(n, device=DEV) for _ in range(2)]
+    if k <= 16384:
+        qg.qgemv_chain(4, [w, w], [Xt[0], Xt[1]], yc, [1, 1])
+        got["chain"] = [yc[0], yc[1]]
+    for B in (2, 8):
+        Y = qg.qgemv_batched(4, w["lo"], None, w["scale"], w["min"], Xt[:B])
+        got[f"batched B={B}"] = [Y[b] for b in range(B)]
+    for name, ys in got.items():
+        for b, yv in enumerate(ys):
+            assert np.array_equal(yv.cpu().numpy().view(np.uint32), want[b].view(np.uint32)), (name, b)

@@ -476,3 +476,84 @@ def test_q2_reconstructs_the_drawn_weights():
     err = np.abs(oracle.dequant(wq) - raw)
     assert np.all(err <= 0.5 * d * (1 + 2.0 ** -9) + 1e-12)
     assert np.max(err / d) > 0.3
+
+
+# ---------------------------------------------------------------- dependent chain
+def _const_w(bits, n, k, code, scale, minv):
+    q = np.full((n, k), code, np.uint8)
+    return make_w(bits, q, np.full((n, k // 32), scale), None if bits == 2 else np.full((n, k // 32), minv))
+
+
+def _const_gemv(c, k, w):
+    """Closed form of a GEMV whose input is the constant fp32 vector c and whose weights
+    are all w: each block has amax |c|, s = fp32(|c| / 127), every code is sign(c)*127,
+    so y_r = k * w * sign(c) * 127 * s for every row (exact in fp64)."""
+    c = np.float32(c)
+    s = np.float32(np.float32(abs(c)) / np.float32(127.0))
+    return float(k) * w * float(np.sign(c)) * 127.0 * float(s)
+
+
+def test_chain_constant_closed_form():
+    # (bits, n, k, code, scale, min, weight value, source)
+    spec = [
+        (4, 96, 64, 3, 0.5, -1.0, 0.5, -1),
+        (4, 32, 96, 1, 0.25, -0.5, -0.25, 0),
+        (6, 64, 32, 40, 0.0625, -2.0, 0.5, 1),
+        (2, 32, 96, 3, 0.75, None, 0.75, 0),  # reads GEMV 0, not the latest output
+    ]
+    mats = [_const_w(b, n, k, c, d, m) for b, n, k, c, d, m, _, _ in spec]
+    src = [t[7] for t in spec]
+    x0 = np.full(64, 0.7, np.float32)
+    outs = oracle.gemv_chain(mats, src, [x0])
+    vals = []
+    for j, (b, n, k, c, d, m, wv, sj) in enumerate(spec):
+        cin = 0.7 if sj < 0 else np.float32(vals[sj])
+        vals.append(_const_gemv(cin, k, wv))
+        assert outs[j].shape == (n,)
+        assert np.all(outs[j] == vals[j]), (j, outs[j][:3], vals[j])
+    assert vals[0] > 0 and vals[1] < 0 and vals[2] < 0 and vals[3] > 0  # signs follow the weights
+    assert len({round(v, 6) for v in vals}) == 4
+
+
+def _random_chain():
+    shapes = [(64, 96), (96, 64), (32, 96), (64, 64)]  # (n, k) per GEMV
+    mats = [datagen.make_quantized(bits, 70 + i, n, k) for i, ((n, k), bits) in enumerate(zip(shapes, (4, 6, 2, 4)))]
+    return mats, [-1, 0, 1, 0]
+
+
+def test_chain_power_of_two_and_sign_equivariance():
+    mats, src = _random_chain()
+    x0 = datagen.normal_f32(71, 1, 96)
+    base = oracle.gemv_chain(mats, src, [x0])
+    four = oracle.gemv_chain(mats, src, [x0 * np.float32(4.0)])
+    neg = oracle.gemv_chain(mats, src, [-x0])
+    for a, b, c in zip(base, four, neg):
+        assert np.array_equal(b, 4.0 * a)
+        assert np.array_equal(c, -a)
+
+
+def test_chain_hands_over_fp32():
+    """A link reads the fp32 rounding of the earlier fp64 output: feeding GEMV 1 that
+    rounding by hand gives the same vector bit for bit, while the chain input differs
+    from the fp64 output itself."""
+    mats, src = _random_chain()
+    x0 = datagen.normal_f32(72, 1, 96)
+    outs = oracle.gemv_chain(mats, src, [x0])
+    assert not np.array_equal(outs[0].astype(np.float32).astype(np.float64), outs[0])
+    assert np.array_equal(oracle.gemv(mats[1], outs[0].astype(np.float32)), outs[1])
+
+
+def test_decode_chain_plan_shapes():
+    """Every link of the decode chain reads a vector of its own k."""
+    from datagen import workloads as W
+
+    src, stages = W.decode_chain_plan(3)
+    assert sum(stages) == len(src) == 21 and stages[:4] == [3, 1, 2, 1]
+    for j, sj in enumerate(src):
+        k = W.PROJ_SHAPES[j % 7][1]
+        n_in = W.HIDDEN if sj < 0 else W.PROJ_SHAPES[sj % 7][0]
+        assert n_in == k, (j, sj)
+        assert sj < j
+    # a link reads only outputs of earlier stages
+    first = np.repeat(np.cumsum([0] + stages[:-1]), stages)
+    assert all(sj < first[j] for j, sj in enumerate(src))

@@ -63,12 +63,40 @@ CASES = {
     "q4_batched_b4_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b8_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
+    "q4_chain_persistent": None,  # the decode chain, --layers layers (run_chain_case)
+    "q4_chain_launches": None,
 }
+
+
+def run_chain_case(args):
+    """Profiling case: the decode chain over the first --layers layers (4 layers: 283 MB,
+    16 phases), --reps calls of qgemv_chain in the mode the case names."""
+    import torch
+
+    import quantized_weight_gemv_gb300 as qg
+    from datagen import workloads as W
+
+    device = torch.device("cuda", 0)
+    src, stages = W.decode_chain_plan(args.layers)
+    mats = [qg.to_device(W.decode_projection(j // 7, j % 7)[0], device) for j in range(len(src))]
+    x0 = torch.from_numpy(W.decode_chain_x()).to(device)
+    ys = [torch.empty(m["n"], device=device) for m in mats]
+    xs = [x0 if s < 0 else ys[s] for s in src]
+    flags = qg.QG_FLAG_CHAIN_LAUNCHES if args.case.endswith("launches") else 0
+    ch = qg.ChainGemv(4, mats, xs, ys, stages, flags=flags)
+    nbytes = sum(W.q4_bytes(m["n"], m["k"]) for m in mats)
+    ms = time_eager(ch.run, torch.cuda.current_stream(device), args.reps)
+    assert qg.device_error() == 0
+    print(json.dumps({"case": args.case, "layers": args.layers, "phases": len(stages), "calls": args.reps,
+                      "us_per_call_eager": ms * 1e3, "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}),
+          flush=True)
 
 
 def run_case(args):
     """A small profiling case: seeded weights of one shape, rotated over copies (> L2), called reps times."""
     import torch
+    if args.case.startswith("q4_chain"):
+        return run_chain_case(args)
 
     import quantized_weight_gemv_gb300 as qg
     from datagen import workloads as W

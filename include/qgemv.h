@@ -272,10 +272,10 @@ int qgemv_grouped_noalloc(int bits, const qg_gemv_desc* descs, int count, unsign
  *   values.  Across phases buffers may be reused freely.
  *   ws : device workspace of at least qg_chain_workspace_bytes(...) bytes, 16-byte
  *        aligned; its first QG_CHAIN_CTL_BYTES bytes are zero-filled once after
- *        allocation and every call that completes leaves them zero.  Calls sharing a
- *        workspace must not overlap on the GPU.
- * Default: one cooperative launch, one CTA per SM, that streams every phase's
- * weights through per-warp bulk-copy rings running ahead across phase boundaries,
+ *        allocation and every call that completes leaves them zero.  Calls sharing a workspace must not
+ *        overlap on the GPU.
+ * Default: one cooperative launch, one CTA per SM, whose producer warp streams every
+ * phase's weights through a bulk-copy ring that runs ahead across phase boundaries,
  * with a grid-wide barrier between phases.  It starts after the preceding work on the
  * stream has finished (QG_FLAG_PDL does not apply to it).  A barrier wait gives up
  * after 1 s: the kernel then records a code in the device error word and stops; the

@@ -8,16 +8,20 @@
 //  * A phase is a list of GEMV descriptors whose inputs all exist before it.  Its work
 //    is cut as in the grouped GEMV: units of 256 blocks of 32 (whole rows), or single
 //    rows of k/8192 such units; CTA b takes the units whose first bulk-copy tile lies
-//    in its equal share of the phase's tiles, warp w every 16th of them from w on.
-//  * Each warp pulls weight tiles through a private ring of cp.async.bulk copies
-//    completed on mbarriers.  Weights do not depend on the chain, so the ring runs
-//    ahead across phase boundaries: while a CTA waits for the others at the end of a
-//    phase, its ring is already filling with the next phase's tiles.
-//  * Between phases: a grid-wide barrier on an arrival counter in the caller's
-//    workspace (fence + atomic add, acquire loads, bounded by %globaltimer, with an
-//    abort word that stops every CTA once one gives up), then every CTA quantises the
-//    next phase's distinct inputs into shared memory, reading them through L2
-//    (ld.global.cg): other SMs wrote them during this launch.
+//    in its equal share of the phase's tiles.
+//  * One producer warp streams the CTA's weight tiles, phase after phase, into a
+//    CTA-wide ring of cp.async.bulk slots (full / empty mbarrier pair per slot).
+//    Weights do not depend on the chain, so the producer never waits for a phase
+//    boundary: while the CTA waits for the others at the end of a phase, the ring
+//    fills with the next phase's tiles, up to ~200 KB ahead.
+//  * Fifteen consumer warps take the phase's units round-robin, read each tile's slot
+//    into registers, release it, and compute as the streaming kernels do.
+//  * Between phases (consumers only, named barrier 1): a grid-wide barrier on an
+//    arrival counter in the caller's workspace (fence + atomic add, acquire loads,
+//    bounded by %globaltimer, with an abort word that stops every CTA once one gives
+//    up), then the consumers quantise the next phase's distinct inputs into shared
+//    memory, reading them through L2 (ld.global.cg): other SMs wrote them during this
+//    launch.
 //  * The last CTA to finish re-arms the counters, so the workspace needs no memset
 //    between calls.
 #include <cstring>
@@ -29,8 +33,9 @@ namespace chain {
 
 using stream::JPL;
 using stream::SBW;
-constexpr int NW = 16;  // warps per CTA
-constexpr int NT = NW * 32;
+constexpr int NC = 15;             // consumer warps
+constexpr int NTC = NC * 32;       // consumer threads
+constexpr int NT = NTC + 32;       // + the producer warp
 
 struct CDesc {
     const uint8_t* lo;
@@ -39,12 +44,13 @@ struct CDesc {
     const uint16_t* min;
     float* y;
     int n;
-    int log2nb;       // log2(k / 32), 5..9
-    int parts;        // tiles per unit
+    int log2nb;       // log2(k / 32), 5..9; a unit has 2^(log2nb-8) tiles when log2nb > 8
     int unit_prefix;  // units of the phase's earlier descriptors
     int tile_prefix;  // tiles of the phase's earlier descriptors
     int img;          // byte offset of its input's activation image in shared memory
 };
+
+__host__ __device__ __forceinline__ int parts_of(int log2nb) { return log2nb > 8 ? 1 << (log2nb - 8) : 1; }
 
 struct CPhase {
     int d0, d1;  // descriptors [d0, d1)
@@ -55,12 +61,12 @@ struct CPhase {
 struct CInput {
     const float* x;
     int k;
-    int img;
+    int img;  // byte offset of its image in shared memory
 };
 
 struct CParams {
     int nphase;
-    int slots;  // ring slots per warp
+    int log2slots;  // log2 of the CTA's ring slots
     unsigned int* err;
     unsigned int* ctl;  // [0] barrier arrivals, [1] abort, [2] CTAs finished
     CDesc d[QG_MAX_GROUP];
@@ -87,64 +93,69 @@ __device__ __forceinline__ int unit_at_tile(const CParams& p, const CPhase& f, l
     if (x >= f.tiles) return f.units;
     const int di = find_in_phase(p, f, (int)x, [](const CDesc& d) { return d.tile_prefix; });
     const CDesc& d = p.d[di];
-    return d.unit_prefix + (int)((x - d.tile_prefix + d.parts - 1) / d.parts);
+    const int parts = parts_of(d.log2nb);
+    return d.unit_prefix + (int)((x - d.tile_prefix + parts - 1) / parts);
 }
 
-// A warp's walk over its tiles: phase, unit within the phase, tile within the unit.
-struct Cursor {
-    int f;
-    int g;
-    int part;
-    int d;
-    int ue;  // end of this CTA's units in phase f
+__device__ __forceinline__ int tile_index(const CDesc& d, int u, int part) {
+    return d.tile_prefix + (u - d.unit_prefix) * parts_of(d.log2nb) + part;
+}
+
+// This CTA's units [ub, ue) of phase f, the phase's index of the first of their tiles
+// and their number.  Called twice per phase, so kept out of line.
+struct Range {
+    int ub, ue, t0, tiles;
 };
 
-// Place c on the warp's first tile of phase f (c.g >= c.ue: the warp has none there).
-// Called about twice per phase and warp, so kept out of line.
-__device__ __noinline__ void cursor_begin(const CParams& p, Cursor& c, int f) {
+__device__ __noinline__ Range cta_range(const CParams& p, int f) {
     const CPhase& ph = p.ph[f];
     const long long T = ph.tiles;
-    const int ub = unit_at_tile(p, ph, T * blockIdx.x / gridDim.x);
-    c.f = f;
-    c.ue = unit_at_tile(p, ph, T * (blockIdx.x + 1) / gridDim.x);
-    c.g = ub + (int)(threadIdx.x >> 5);
-    c.part = 0;
-    c.d = c.g < c.ue ? find_in_phase(p, ph, c.g, [](const CDesc& d) { return d.unit_prefix; }) : ph.d0;
+    Range r;
+    r.ub = unit_at_tile(p, ph, T * blockIdx.x / gridDim.x);
+    r.ue = unit_at_tile(p, ph, T * (blockIdx.x + 1) / gridDim.x);
+    auto first_tile = [&](int u) {
+        if (u >= ph.units) return ph.tiles;
+        const int di = find_in_phase(p, ph, u, [](const CDesc& d) { return d.unit_prefix; });
+        return tile_index(p.d[di], u, 0);
+    };
+    r.t0 = first_tile(r.ub);
+    r.tiles = first_tile(r.ue) - r.t0;
+    return r;
 }
 
-// next tile of the warp within the phase (c.g >= c.ue once its share is done)
-__device__ __forceinline__ void cursor_next(const CParams& p, Cursor& c) {
-    if (++c.part == p.d[c.d].parts) {
-        c.part = 0;
-        c.g += NW;
-        const int d1 = p.ph[c.f].d1;
-        while (c.d + 1 < d1 && c.g >= p.d[c.d + 1].unit_prefix) ++c.d;
-    }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(stream::smem_u32(bar)) : "memory");
 }
 
-// Move on to the next phase that holds a tile for this warp (c.f == nphase: none
-// left).  The phase index is carried in a local and the end marker written once,
-// after the loop.
-__device__ __forceinline__ void cursor_settle(const CParams& p, Cursor& c) {
-    int f = c.f;
-    while (f < p.nphase && c.g >= c.ue) {
-        ++f;
-        if (f < p.nphase) cursor_begin(p, c, f);
+// named barrier of the consumer warps (the producer warp never joins it)
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"r"(NTC) : "memory"); }
+
+// Producer: wait until the slot's previous tile has been read.  False when the CTA
+// is stopping (abort flag) or after WAIT_LIMIT_NS.
+__device__ bool wait_empty(uint64_t* bar, uint32_t parity, const volatile int* abort_flag, unsigned int* err) {
+    if (stream::mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (stream::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(err, ERR_WAIT_EMPTY);
+            return false;
+        }
     }
-    c.f = f;
 }
 
 template <int BITS>
-__device__ __forceinline__ void issue_tile(const CParams& p, const Cursor& c, unsigned char* slot, uint64_t* bar,
+__device__ __forceinline__ void issue_tile(const CDesc& d, int ul, int part, unsigned char* slot, uint64_t* bar,
                                            uint64_t pol) {
     using SL = stream::Slot<BITS>;
-    const CDesc& d = p.d[c.d];
-    const int nb = 1 << d.log2nb;
-    const int R = nb >= SBW ? 1 : SBW / nb;
-    const int ul = c.g - d.unit_prefix;
-    const int rows_u = R == 1 ? 1 : min(R, d.n - ul * R);
-    const uint32_t blocks = (uint32_t)(nb >= SBW ? SBW : rows_u * nb);
-    const size_t blk0 = (size_t)ul * R * nb + (size_t)c.part * SBW;
+    const int l = d.log2nb;
+    const int lr = l >= 8 ? 0 : 8 - l;  // log2 of the rows per unit (256 blocks per tile)
+    const int rows_u = min(1 << lr, d.n - (ul << lr));
+    const uint32_t blocks = l >= 8 ? (uint32_t)SBW : (uint32_t)rows_u << l;
+    const size_t blk0 = ((size_t)ul << (lr + l)) + (size_t)part * SBW;
     stream::mbar_arrive_expect_tx(bar, blocks * SL::BPB);
     stream::bulk_g2s(slot, d.lo + blk0 * SL::CODE, blocks * SL::CODE, bar, pol);
     if constexpr (BITS == 6) stream::bulk_g2s(slot + SL::HI, d.hi + blk0 * 8, blocks * 8, bar, pol);
@@ -210,8 +221,8 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned int* p) {
 // Thread 0 of each CTA: arrive, then wait until `target` arrivals (all CTAs of this
 // and every earlier boundary).  False when the wait ran out or another CTA gave up.
 __device__ bool grid_barrier(const CParams& p, unsigned target) {
-    __threadfence();  // the CTA's outputs (ordered before by __syncthreads) before the arrival
-    atomicAdd(p.ctl, 1u);
+    // release: the CTA's outputs (ordered before by the consumers' barrier) before the arrival
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.ctl) : "memory");
     if (ld_acquire_gpu(p.ctl) >= target) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (;;) {
@@ -227,124 +238,180 @@ __device__ bool grid_barrier(const CParams& p, unsigned target) {
     }
 }
 
+// byte offsets of the shared-memory regions: ring | full[NS] | empty[NS] | image
+__host__ __device__ constexpr size_t chain_full_off(int ns, int slot_bytes) { return (size_t)ns * slot_bytes; }
+__host__ __device__ constexpr size_t chain_img_off(int ns, int slot_bytes) {
+    return ((size_t)ns * (slot_bytes + 16) + 15) & ~(size_t)15;
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CParams p) {
     using SL = stream::Slot<BITS>;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_abort;
+    __shared__ volatile int s_abort;
+    __shared__ Range s_range[QG_MAX_GROUP];  // this CTA's share of every phase
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int D = p.slots;
-    unsigned char* slots = smem + (size_t)warp * D * SL::BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NW * D * SL::BYTES) + warp * D;
-    unsigned char* img = smem + stream::xq_offset(NW * D, SL::BYTES);
-    const uint64_t pol = stream::policy_evict_first();
+    const int NS = 1 << p.log2slots;
+    const int LS = p.log2slots;
+    unsigned char* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + chain_full_off(NS, SL::BYTES));
+    uint64_t* empty = full + NS;
+    unsigned char* img = smem + chain_img_off(NS, SL::BYTES);
 
-    if (threadIdx.x == 0) s_abort = 0;
-    Cursor ic;  // issue cursor, lane 0 only
-    int issued = 0;
-    if (lane == 0) {
-        for (int s = 0; s < D; ++s) stream::mbar_init(&full[s], 1);
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < NS; ++i) {
+            stream::mbar_init(&full[i], 1);
+            stream::mbar_init(&empty[i], 1);
+        }
         stream::fence_mbar_init();
-        cursor_begin(p, ic, 0);
-        cursor_settle(p, ic);
-        while (issued < D && ic.f < p.nphase) {
-            issue_tile<BITS>(p, ic, slots + (size_t)(issued % D) * SL::BYTES, &full[issued % D], pol);
-            ++issued;
-            cursor_next(p, ic);
-            cursor_settle(p, ic);
-        }
     }
-    __syncwarp();
+    // the ranges need dependent reads of the parameter block: all phases at once, here
+    for (int f = threadIdx.x; f < p.nphase; f += NT) s_range[f] = cta_range(p, f);
+    __syncthreads();
 
-    int t = 0;  // tiles consumed by this warp
-    for (int f = 0; f < p.nphase; ++f) {
-        // ---- phase boundary.  Every thread takes each __syncthreads below the same
-        // number of times: s_abort only changes between the first two (thread 0) or
-        // after the third (a warp whose tile never landed), and is read between the
-        // second and the third.
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            if (s_abort)
-                atomicExch(p.ctl + 1, 1u);
-            else if (f > 0 && !grid_barrier(p, gridDim.x * (unsigned)f))
-                s_abort = 1;
-        }
-        __syncthreads();
-        if (s_abort) break;
-        const CPhase& ph = p.ph[f];
-        for (int i = ph.in0; i < ph.in1; ++i)
-            quantize_x_cols<NT, true>(p.in[i].x, p.in[i].k, 1, img + p.in[i].img, 0, threadIdx.x);
-        __syncthreads();
-
-        Cursor cc;
-        cursor_begin(p, cc, f);
-        float rowacc = 0.0f;
-        while (cc.g < cc.ue) {
-            const int slot = t % D;
-            // all lanes poll; the decision is taken together so that the warp stays converged
-            if (!__all_sync(0xffffffffu, stream::mbar_wait(&full[slot], (uint32_t)((t / D) & 1)))) {
-                if (lane == 0) atomicOr(p.err, ERR_WAIT_FULL);
-                s_abort = 1;
-                break;
+    if (warp == NC) {
+        // ---------------- producer: every tile of the CTA, phase after phase.  The warp
+        // walks the tile sequence together; each batch of up to 8 tiles is issued by
+        // lanes 0-7 at once, lane i taking the batch's i-th tile.
+        const uint64_t pol = stream::policy_evict_first();
+        int f = 0, u = 0, ue = 0, di = 0, part = 0;  // walk cursor (the same in every lane)
+        auto enter = [&](int from) {                  // first phase >= from with a tile here
+            for (f = from; f < p.nphase; ++f) {
+                const Range r = s_range[f];
+                if (r.ub < r.ue) {
+                    u = r.ub;
+                    ue = r.ue;
+                    di = find_in_phase(p, p.ph[f], u, [](const CDesc& d) { return d.unit_prefix; });
+                    part = 0;
+                    return;
+                }
             }
-            const unsigned char* st = slots + (size_t)slot * SL::BYTES;
-            uint4 cw[JPL];
-            uint2 hw[JPL];
-            unsigned short dh[JPL], mh[JPL];
+        };
+        enter(0);
+        int n = 0;  // tiles issued
+        bool stop = false;
+        while (!stop && f < p.nphase) {
+            int my_di = 0, my_ul = 0, my_part = 0, cnt = 0;
+            for (; cnt < 8 && f < p.nphase; ++cnt) {
+                if (lane == cnt) {
+                    my_di = di;
+                    my_ul = u - p.d[di].unit_prefix;
+                    my_part = part;
+                }
+                if (++part == parts_of(p.d[di].log2nb)) {
+                    part = 0;
+                    if (++u == ue) {
+                        enter(f + 1);
+                    } else {
+                        while (di + 1 < p.ph[f].d1 && u >= p.d[di + 1].unit_prefix) ++di;
+                    }
+                }
+            }
+            const int m = n + lane;
+            const int slot = m & (NS - 1);
+            bool ok = true;
+            // The first pass over the ring finds every slot free (parity 1 of a fresh
+            // barrier).  The consumer's arrive on `empty` releases its reads of the slot;
+            // this wait acquires them before the copy overwrites it.
+            if (lane < cnt) ok = wait_empty(&empty[slot], (uint32_t)(((m >> LS) & 1) ^ 1), &s_abort, p.err);
+            stop = __any_sync(0xffffffffu, !ok);
+            if (!stop && lane < cnt)
+                issue_tile<BITS>(p.d[my_di], my_ul, my_part, ring + (size_t)slot * SL::BYTES, &full[slot], pol);
+            if (!stop) n += cnt;
+        }
+        // copies in flight land before the CTA exits (the last NS issued)
+        if (lane == 0) {
+            for (int m = n > NS ? n - NS : 0; m < n; ++m) {
+                if (!stream::mbar_wait(&full[m & (NS - 1)], (uint32_t)((m >> LS) & 1))) {
+                    atomicOr(p.err, ERR_WAIT_DRAIN);
+                    break;
+                }
+            }
+        }
+    } else {
+        // ---------------- consumers
+        int base = 0;  // tiles of this CTA in earlier phases
+        for (int f = 0; f < p.nphase; ++f) {
+            // Phase boundary.  The consumers take each consumer_sync the same number of
+            // times: s_abort changes only between the first two (thread 0) or after the
+            // third (a warp whose tile never landed) and is read between the second and
+            // the third.
+            const CPhase& ph = p.ph[f];
+            consumer_sync();
+            if (threadIdx.x == 0) {
+                if (s_abort)
+                    atomicExch(p.ctl + 1, 1u);
+                else if (f > 0 && !grid_barrier(p, gridDim.x * (unsigned)f))
+                    s_abort = 1;
+            }
+            consumer_sync();
+            if (s_abort) break;
+            for (int i = ph.in0; i < ph.in1; ++i)
+                quantize_x_cols<NTC, true>(p.in[i].x, p.in[i].k, 1, img + p.in[i].img, 0, threadIdx.x);
+            consumer_sync();
+
+            const Range r = s_range[f];
+            float rowacc = 0.0f;
+            bool bad = false;
+            int di = ph.d0;
+            for (int u = r.ub + warp; u < r.ue && !bad; u += NC) {
+                while (di + 1 < ph.d1 && u >= p.d[di + 1].unit_prefix) ++di;
+                const CDesc& d = p.d[di];
+                const int ul = u - d.unit_prefix;
+                const int parts = parts_of(d.log2nb);
+                for (int part = 0; part < parts; ++part) {
+                    const int n = base + tile_index(d, u, part) - r.t0;
+                    const int slot = n & (NS - 1);
+                    // all lanes poll; the decision is taken together so that the warp stays converged
+                    if (!__all_sync(0xffffffffu, stream::mbar_wait(&full[slot], (uint32_t)((n >> LS) & 1)))) {
+                        if (lane == 0) atomicOr(p.err, ERR_WAIT_FULL);
+                        s_abort = 1;
+                        bad = true;
+                        break;
+                    }
+                    const unsigned char* st = ring + (size_t)slot * SL::BYTES;
+                    uint4 cw[JPL];
+                    uint2 hw[JPL];
+                    unsigned short dh[JPL], mh[JPL];
 #pragma unroll
-            for (int j = 0; j < JPL; ++j) {
-                const int fb = lane + 32 * j;
-                cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
-                if constexpr (BITS == 6)
-                    hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
-                else
-                    hw[j] = make_uint2(0u, 0u);
-                dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
-                mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
-            }
-            __syncwarp();
-            if (lane == 0 && ic.f < p.nphase) {
-                stream::fence_proxy_async();  // the slot's generic reads are done before the refill
-                issue_tile<BITS>(p, ic, slots + (size_t)(issued % D) * SL::BYTES, &full[issued % D], pol);
-                ++issued;
-                cursor_next(p, ic);
-                cursor_settle(p, ic);
-            }
-            ++t;
+                    for (int j = 0; j < JPL; ++j) {
+                        const int fb = lane + 32 * j;
+                        cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
+                        if constexpr (BITS == 6)
+                            hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+                        else
+                            hw[j] = make_uint2(0u, 0u);
+                        dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
+                        mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[slot]);  // the slot may be refilled
 
-            const CDesc& d = p.d[cc.d];
-            const unsigned char* xim = img + d.img;
-            const int ul = cc.g - d.unit_prefix;
-            switch (d.log2nb) {
-                case 5:
-                    tile_compute<BITS, 5>(d, xim, ul, cc.part, cw, hw, dh, mh, rowacc);
-                    break;
-                case 6:
-                    tile_compute<BITS, 6>(d, xim, ul, cc.part, cw, hw, dh, mh, rowacc);
-                    break;
-                case 7:
-                    tile_compute<BITS, 7>(d, xim, ul, cc.part, cw, hw, dh, mh, rowacc);
-                    break;
-                case 8:
-                    tile_compute<BITS, 8>(d, xim, ul, cc.part, cw, hw, dh, mh, rowacc);
-                    break;
-                default:
-                    tile_compute<BITS, 9>(d, xim, ul, cc.part, cw, hw, dh, mh, rowacc);
-                    break;
+                    const unsigned char* xim = img + d.img;
+                    switch (d.log2nb) {
+                        case 5:
+                            tile_compute<BITS, 5>(d, xim, ul, part, cw, hw, dh, mh, rowacc);
+                            break;
+                        case 6:
+                            tile_compute<BITS, 6>(d, xim, ul, part, cw, hw, dh, mh, rowacc);
+                            break;
+                        case 7:
+                            tile_compute<BITS, 7>(d, xim, ul, part, cw, hw, dh, mh, rowacc);
+                            break;
+                        case 8:
+                            tile_compute<BITS, 8>(d, xim, ul, part, cw, hw, dh, mh, rowacc);
+                            break;
+                        default:
+                            tile_compute<BITS, 9>(d, xim, ul, part, cw, hw, dh, mh, rowacc);
+                            break;
+                    }
+                }
             }
-            cursor_next(p, cc);
+            base += r.tiles;
         }
     }
 
-    // ---- stopping early: let this warp's copies in flight land before the CTA exits
-    if (lane == 0) {
-        for (int u = t; u < issued; ++u) {
-            if (!stream::mbar_wait(&full[u % D], (uint32_t)((u / D) & 1))) {
-                atomicOr(p.err, ERR_WAIT_DRAIN);
-                break;
-            }
-        }
-    }
     // ---- the last CTA out re-arms the counters for the next call
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -429,12 +496,12 @@ int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phas
             d.log2nb = l;
             d.img = p.in[in].img;
             const int R = nb >= 256 ? 1 : 256 / nb;
-            d.parts = nb > 256 ? nb / 256 : 1;
+            const int parts = parts_of(l);
             const long long du = nb >= 256 ? s.n : (s.n + R - 1) / R;
             d.unit_prefix = (int)units;
             d.tile_prefix = (int)tiles;
             units += du;
-            tiles += du * d.parts;
+            tiles += du * parts;
         }
         off += phase_sizes[f];
         if (m == P.d0) continue;  // nothing to compute: no boundary needed
@@ -451,13 +518,14 @@ int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phas
     p.err = lc.err;
     p.ctl = reinterpret_cast<unsigned int*>(ws);
 
+    // the ring takes what the activation images leave of the opt-in shared memory
     const int slot = bits == 4 ? stream::Slot<4>::BYTES : stream::Slot<6>::BYTES;
-    const size_t cap = (size_t)lc.max_smem_optin - 1024;
-    int D = 4;
-    while (D > 1 && stream::xq_offset(NW * D, slot) + (size_t)img_max > cap) --D;
-    const size_t smem = stream::xq_offset(NW * D, slot) + (size_t)img_max;
+    const size_t cap = (size_t)lc.max_smem_optin - 1024 - sizeof(Range) * QG_MAX_GROUP - 128;
+    int ls = 6;  // a power of two number of slots, at most 64
+    while (ls > 1 && chain_img_off(1 << ls, slot) + (size_t)img_max > cap) --ls;
+    const size_t smem = chain_img_off(1 << ls, slot) + (size_t)img_max;
     if (smem > cap) return QG_ERR_UNSUPPORTED;
-    p.slots = D;
+    p.log2slots = ls;
     const void* kern = bits == 4 ? (const void*)chain_kernel<4> : (const void*)chain_kernel<6>;
     if (int e = ensure_smem_attr(kern, smem, lc)) return e;
     int per_sm = 0;

@@ -60,12 +60,16 @@ __device__ __forceinline__ float half_bits_to_float(unsigned short b) {
 // two can round to different integers only when t lies within ~2.3e-5 of a
 // half-integer.  Outside 1/4096 of one, rint(t) is the answer; inside (and for a NaN
 // or infinite t) the exact quotient decides.
+// The nearest integer to t comes from fp32 adds: t + 1.5*2^23 rounds to an integer
+// (round-half-even, |t| < 2^22) whose value sits in the low mantissa bits.
 __device__ __forceinline__ int quant_code(float x, float s, float inv) {
+    constexpr float MAGIC = 12582912.0f;  // 1.5 * 2^23
     const float t = x * inv;
-    const float a = fabsf(t);
+    const float r = __fadd_rn(t, MAGIC);
+    const float qf = __fsub_rn(r, MAGIC);
     int q;
-    if (fabsf(a - floorf(a) - 0.5f) > (1.0f / 4096.0f))
-        q = __float2int_rn(t);
+    if (fabsf(t - qf) < 0.5f - (1.0f / 4096.0f))
+        q = __float_as_int(r) - 0x4B400000;
     else
         q = __float2int_rn(__fdiv_rn(x, s));
     return max(-127, min(127, q));

@@ -32,7 +32,7 @@ METRIC = "effective weight GB/s & GEMV/s at batch 1 (fraction of ~8 TB/s HBM)"
 # full decode-layer stream (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None
 # whenever the kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "grouped": None,
+    "grouped": {"kernel": "grouped::grouped_gemv_kernel<4,2,0>", "bytes_per_launch": 2484.06e6},
     "percall": None,
 }
 
@@ -82,7 +82,7 @@ def run_chain_case(args):
     x0 = torch.from_numpy(W.decode_chain_x()).to(device)
     ys = [torch.empty(m["n"], device=device) for m in mats]
     xs = [x0 if s < 0 else ys[s] for s in src]
-    flags = qg.QG_FLAG_CHAIN_LAUNCHES if args.case.endswith("launches") else 0
+    flags = qg.QG_FLAG_CHAIN_PERSISTENT if args.case.endswith("persistent") else 0
     ch = qg.ChainGemv(4, mats, xs, ys, stages, flags=flags)
     nbytes = sum(W.q4_bytes(m["n"], m["k"]) for m in mats)
     ms = time_eager(ch.run, torch.cuda.current_stream(device), args.reps)
@@ -272,6 +272,17 @@ def time_eager(fn, stream, reps, warm=3):
     return e0.elapsed_time(e1) / reps
 
 
+def ch_launches(stages, flags):
+    """Kernel launches per call of the decode chain: the persistent kernel is one; the
+    per-phase mode is one per phase whose input is short (q/k/v, o, gate/up: 2048
+    values) and two for the down projection's 16384-value input."""
+    import quantized_weight_gemv_gb300 as qg
+
+    if flags & qg.QG_FLAG_CHAIN_PERSISTENT:
+        return 1
+    return sum(2 if i % 4 == 3 else 1 for i in range(len(stages)))
+
+
 def decode_chain_rows(mats, n_layers, total_bytes, stream, reps):
     """The decode chain on the same weights: every GEMV reads an earlier one's output
     (q, k, v <- layer input; o <- q; gate, up <- o; down <- gate; next layer <- down),
@@ -287,7 +298,7 @@ def decode_chain_rows(mats, n_layers, total_bytes, stream, reps):
     x0 = torch.from_numpy(W.decode_chain_x()).to(device)
     xc = [x0 if s < 0 else yc[s] for s in src]
     out = {"phases": len(stages), "gemvs": len(src)}
-    for name, fl, launches in (("persistent", 0, 1), ("launches", qg.QG_FLAG_CHAIN_LAUNCHES, 2 * len(stages))):
+    for name, fl in (("launches", 0), ("persistent", qg.QG_FLAG_CHAIN_PERSISTENT)):
         ch = qg.ChainGemv(4, mats, xc, yc, stages, flags=fl)
         try:
             g = graph_of(ch.run, stream)
@@ -299,7 +310,8 @@ def decode_chain_rows(mats, n_layers, total_bytes, stream, reps):
             ms = time_eager(ch.run, stream, reps)
             how = f"eager ({type(e).__name__})"
         out[name] = {"us_per_token": ms * 1e3, "GBps": total_bytes / (ms * 1e-3) / 1e9,
-                     "us_per_phase": ms * 1e3 / len(stages), "launches_per_token": launches, "timed_as": how}
+                     "us_per_phase": ms * 1e3 / len(stages), "launches_per_token": ch_launches(stages, fl),
+                     "timed_as": how}
     assert qg.device_error() == 0
     return out
 

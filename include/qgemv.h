@@ -62,9 +62,8 @@ enum qg_status {
                                writing any output or touching the workspace.  The caller     \
                                guarantees that no preceding work writes the weights.         */
 #define QG_FLAG_PLAIN 0x2u  /* force the plain-load kernel (128-bit loads, no bulk-copy ring) */
-#define QG_FLAG_CHAIN_LAUNCHES 0x4u /* qgemv_chain: one grouped launch pair per phase, chained by  \
-                                       programmatic dependent launch, instead of one persistent    \
-                                       cooperative launch                                          */
+#define QG_FLAG_CHAIN_PERSISTENT 0x4u /* qgemv_chain: one persistent cooperative launch for all  \
+                                         phases instead of per-phase launches                     */
 
 /* Largest supported sizes. */
 #define QG_MAX_K 65536       /* qgemv_q4/q6 and vocab: k <= QG_MAX_K */
@@ -274,14 +273,16 @@ int qgemv_grouped_noalloc(int bits, const qg_gemv_desc* descs, int count, unsign
  *        aligned; its first QG_CHAIN_CTL_BYTES bytes are zero-filled once after
  *        allocation and every call that completes leaves them zero.  Calls sharing a workspace must not
  *        overlap on the GPU.
- * Default: one cooperative launch, one CTA per SM, whose producer warp streams every
- * phase's weights through a bulk-copy ring that runs ahead across phase boundaries,
- * with a grid-wide barrier between phases.  It starts after the preceding work on the
- * stream has finished (QG_FLAG_PDL does not apply to it).  A barrier wait gives up
- * after 1 s: the kernel then records a code in the device error word and stops; the
- * outputs are undefined.  With QG_FLAG_CHAIN_LAUNCHES each phase runs as the two
- * launches of qgemv_grouped instead, phase f+1 chained to phase f by programmatic
- * dependent launch (QG_FLAG_PDL applies to the first phase).
+ * Default: each phase runs as qgemv_grouped's launches, phase f+1 chained to phase f
+ * by programmatic dependent launch (QG_FLAG_PDL applies to the first phase); a phase
+ * whose distinct inputs are short (6144 values in all) is one launch whose CTAs
+ * quantise the inputs themselves.  With QG_FLAG_CHAIN_PERSISTENT: one cooperative
+ * launch, one CTA per SM, whose producer warp streams every phase's weights through
+ * a bulk-copy ring that runs ahead across phase boundaries, with a grid-wide barrier
+ * between phases.  That launch starts after the preceding work on the stream has
+ * finished (QG_FLAG_PDL does not apply to it).  A barrier wait gives up after 1 s: the
+ * kernel then records a code in the device error word and stops; the outputs are
+ * undefined.
  */
 #define QG_CHAIN_CTL_BYTES 256
 #define QG_CHAIN_MAX_PHASE_K 32768

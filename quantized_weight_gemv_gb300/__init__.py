@@ -25,7 +25,7 @@ QG_ERR_CUDA = -5
 
 QG_FLAG_PDL = 0x1
 QG_FLAG_PLAIN = 0x2
-QG_FLAG_CHAIN_LAUNCHES = 0x4
+QG_FLAG_CHAIN_PERSISTENT = 0x4
 QG_CHAIN_CTL_BYTES = 256
 QG_CHAIN_MAX_PHASE_K = 32768
 

@@ -443,7 +443,7 @@ int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phas
                  unsigned char* ws, const LaunchCtx& lc) {
     using namespace chain;
     (void)count;
-    if (lc.flags & QG_FLAG_CHAIN_LAUNCHES) {
+    if (!(lc.flags & QG_FLAG_CHAIN_PERSISTENT)) {  // one grouped launch (pair) per phase
         int off = 0;
         bool launched = false;
         for (int f = 0; f < nphase; ++f) {
@@ -452,7 +452,7 @@ int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phas
             bool any = false;
             for (int i = off; i < off + phase_sizes[f]; ++i) any = any || descs[i].n > 0;
             if (any) {
-                const int rc = launch_grouped(bits, descs + off, phase_sizes[f], ws + QG_CHAIN_CTL_BYTES, l2);
+                const int rc = launch_grouped(bits, descs + off, phase_sizes[f], ws + QG_CHAIN_CTL_BYTES, l2, true);
                 if (rc != QG_OK) return rc;
                 launched = true;
             }

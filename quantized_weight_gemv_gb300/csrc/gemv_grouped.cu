@@ -7,6 +7,8 @@
 // x, y, n, k), passed by value as the kernel parameter, so nothing is allocated:
 //  1. grouped_quantize_kernel: every activation of the group, quantised per block
 //     of 32 (one warp per block) into the caller's workspace;
+//     (A group whose distinct activations are short may skip this launch: the GEMV
+//     kernel then quantises them itself into shared memory, see SMX below.)
 //  2. grouped_gemv_kernel (programmatic dependent launch on 1): persistent CTAs
 //     split the concatenated work of all descriptors - units of 256 blocks (whole
 //     rows), or single rows of k/8192 such units for k > 8192 - into contiguous,
@@ -38,6 +40,13 @@ struct GDesc {
     int stage_prefix;  // stages of the descriptors before
     int qb_prefix;     // activation blocks of the descriptors before
     int ws_off;        // byte offset of this descriptor's activation image in the workspace
+                       // (SMX: in the kernel's shared-memory image area)
+};
+
+struct GInput {  // a distinct activation of an SMX group and its shared-memory image
+    const float* x;
+    int k;
+    int off;
 };
 
 struct GParams {
@@ -48,8 +57,20 @@ struct GParams {
     int stages_per_warp;
     unsigned int* err;
     unsigned char* ws;
+    int nin;        // SMX: distinct activations, quantised by every CTA after griddepcontrol.wait
+    int img_bytes;  // SMX: bytes of their shared-memory images
     GDesc d[QG_MAX_GROUP];
+    GInput in[QG_MAX_GROUP];
 };
+
+// activation image reads: the workspace through the read-only path, or shared memory
+template <bool SMX, typename T>
+__device__ __forceinline__ T ldx(const T* ptr) {
+    if constexpr (SMX)
+        return *ptr;
+    else
+        return __ldg(ptr);
+}
 
 // descriptor holding global index v of a prefix array (largest d with prefix <= v)
 template <typename F>
@@ -76,7 +97,7 @@ __global__ void __launch_bounds__(256) grouped_quantize_kernel(const __grid_cons
         const int nb = 1 << d.log2nb;
         float s;
         int S;
-        const int q = quantize_lane(d.x[32 * b + lane], s, S);
+        const int q = quantize_lane(__ldcg(d.x + 32 * b + lane), s, S);
         const XqView v = xq_view(p.ws + d.ws_off, nb);
         if (lane < 16)
             v.lo[16 * b + lane] = (int8_t)q;
@@ -112,7 +133,7 @@ __device__ __forceinline__ int unit_at_stage(const GParams& p, int x) {
     return d.unit_prefix + local;
 }
 
-template <int BITS, int L>
+template <int BITS, int L, bool SMX>
 __device__ __forceinline__ void stage_compute(const GDesc& d, const unsigned char* xqws, int unit_local, int part,
                                               const uint4 (&cw)[JPL], const uint2 (&hw)[JPL],
                                               const unsigned short (&dh)[JPL], const unsigned short (&mh)[JPL],
@@ -140,9 +161,9 @@ __device__ __forceinline__ void stage_compute(const GDesc& d, const unsigned cha
             r = block_combine(qdot<BITS>(cw[j], hw[j], xl[xj], xh[xj]), dd, mm, xs[xj], xS[xj]);
         } else {
             const int blk = (part * SBW + lane + 32 * j) & (NB - 1);
-            const uint4 a = __ldg(reinterpret_cast<const uint4*>(v.lo + 16 * blk));
-            const uint4 b = __ldg(reinterpret_cast<const uint4*>(v.hi + 16 * blk));
-            r = block_combine(qdot<BITS>(cw[j], hw[j], a, b), dd, mm, __ldg(v.s + blk), __ldg(v.S + blk));
+            const uint4 a = ldx<SMX>(reinterpret_cast<const uint4*>(v.lo + 16 * blk));
+            const uint4 b = ldx<SMX>(reinterpret_cast<const uint4*>(v.hi + 16 * blk));
+            r = block_combine(qdot<BITS>(cw[j], hw[j], a, b), dd, mm, ldx<SMX>(v.s + blk), ldx<SMX>(v.S + blk));
         }
         pj[j] = rloc < rows_u ? r : 0.0f;
     }
@@ -169,7 +190,9 @@ __device__ __forceinline__ void stage_compute(const GDesc& d, const unsigned cha
     }
 }
 
-template <int BITS, int MINB>
+// SMX: the group's activations are quantised by each CTA into shared memory (after
+// the ring slots) instead of being read from the workspace kernel 1 filled.
+template <int BITS, int MINB, bool SMX>
 __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_constant__ GParams p) {
     using SL = stream::Slot<BITS>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -220,6 +243,12 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
     }
     __syncwarp();
     pdl_wait();  // the activation images and the outputs depend on the preceding kernel
+    unsigned char* const xbase = SMX ? smem + stream::xq_offset(8 * D, SL::BYTES) : p.ws;
+    if constexpr (SMX) {
+        for (int i = 0; i < p.nin; ++i)
+            quantize_x_cols<256, true>(p.in[i].x, p.in[i].k, 1, xbase + p.in[i].off, 0, threadIdx.x);
+        __syncthreads();
+    }
 
     uint4 xl[2], xh[2];
     float xs[2], xS[2];
@@ -255,41 +284,44 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
         }
 
         const GDesc& d = p.d[cc.d];
-        const unsigned char* xqws = p.ws + d.ws_off;
+        const unsigned char* xqws = xbase + d.ws_off;
         if (d.log2nb <= 6 && xd != cc.d) {  // activation words of a new descriptor
             const int nb = 1 << d.log2nb;
             const XqView v = xq_view(const_cast<unsigned char*>(xqws), nb);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int blk = min(lane + 32 * j, nb - 1);
-                xl[j] = __ldg(reinterpret_cast<const uint4*>(v.lo + 16 * blk));
-                xh[j] = __ldg(reinterpret_cast<const uint4*>(v.hi + 16 * blk));
-                xs[j] = __ldg(v.s + blk);
-                xS[j] = __ldg(v.S + blk);
+                xl[j] = ldx<SMX>(reinterpret_cast<const uint4*>(v.lo + 16 * blk));
+                xh[j] = ldx<SMX>(reinterpret_cast<const uint4*>(v.hi + 16 * blk));
+                xs[j] = ldx<SMX>(v.s + blk);
+                xS[j] = ldx<SMX>(v.S + blk);
             }
             xd = cc.d;
         }
         const int ul = cc.g - d.unit_prefix;
         switch (d.log2nb) {
             case 5:
-                stage_compute<BITS, 5>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                stage_compute<BITS, 5, SMX>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
                 break;
             case 6:
-                stage_compute<BITS, 6>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                stage_compute<BITS, 6, SMX>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
                 break;
             case 7:
-                stage_compute<BITS, 7>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                stage_compute<BITS, 7, SMX>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
                 break;
             case 8:
-                stage_compute<BITS, 8>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                stage_compute<BITS, 8, SMX>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
                 break;
             default:
-                stage_compute<BITS, 9>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
+                stage_compute<BITS, 9, SMX>(d, xqws, ul, cc.part, cw, hw, dh, mh, xl, xh, xs, xS, rowacc);
                 break;
         }
         cc.advance(p);
     }
 }
+
+// fused form: distinct activations of at most this many image bytes (k <= 6144 in total)
+constexpr int SMX_MAX_IMAGE = 7680;
 
 static int env_int(const char* name, int dflt) {
     const char* v = getenv(name);
@@ -305,7 +337,8 @@ size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count) {
     return off;
 }
 
-int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc) {
+int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc,
+                   bool fuse) {
     using namespace grouped;
     static_assert(sizeof(GParams) < 32000, "grouped parameters must fit the kernel parameter space");
     GParams p;
@@ -348,45 +381,71 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
     p.err = lc.err;
     p.ws = ws;
 
-    // 1. activations
-    long long qgrid = (qblocks + 7) / 8;
-    if (qgrid > lc.sm_count * 16) qgrid = lc.sm_count * 16;
-    int rc = launch_kernel(grouped_quantize_kernel, dim3((unsigned)qgrid), dim3(256), 0, lc, p);
-    if (rc != QG_OK) return rc;
+    // Fused form: when the group's distinct activations (by x and k) are short, every
+    // CTA quantises them itself into shared memory after griddepcontrol.wait and the
+    // quantisation launch is skipped - one dependent launch instead of two.
+    bool smx = false;
+    if (fuse) {
+        int ni = 0, ioff = 0, woff[QG_MAX_GROUP];
+        for (int i = 0; i < m && ioff <= SMX_MAX_IMAGE; ++i) {
+            const int k = 32 << p.d[i].log2nb;
+            int j = 0;
+            while (j < ni && !(p.in[j].x == p.d[i].x && p.in[j].k == k)) ++j;
+            if (j == ni) {
+                p.in[ni].x = p.d[i].x;
+                p.in[ni].k = k;
+                p.in[ni].off = ioff;
+                ioff += xq_stride(k >> 5);
+                ++ni;
+            }
+            woff[i] = p.in[j].off;
+        }
+        if (ioff <= SMX_MAX_IMAGE) {
+            smx = true;
+            p.nin = ni;
+            p.img_bytes = ioff;
+            for (int i = 0; i < m; ++i) p.d[i].ws_off = woff[i];
+        }
+    }
 
-    // 2. the GEMVs, always chained to 1 by programmatic dependent launch.  Default:
-    // two CTAs per SM (16 warps, at most 128 registers each) and one ring slot per
-    // warp - measured on GB300 as the fastest shape: the slot is refilled as soon as
-    // it has been copied to registers, so 16 x 5 KB stay in flight per SM.  The
-    // diagnostic switches QG_GROUPED_CTAS_PER_SM (1 or 2) and QG_GROUPED_SLOTS
-    // (slots per warp) override it.
+    // 1. activations
+    if (!smx) {
+        long long qgrid = (qblocks + 7) / 8;
+        if (qgrid > lc.sm_count * 16) qgrid = lc.sm_count * 16;
+        int rc = launch_kernel(grouped_quantize_kernel, dim3((unsigned)qgrid), dim3(256), 0, lc, p);
+        if (rc != QG_OK) return rc;
+    }
+
+    // 2. the GEMVs, chained to 1 by programmatic dependent launch (fused form: the
+    // caller's flags).  Default: two CTAs per SM (16 warps, at most 128 registers each)
+    // and one ring slot per warp - measured on GB300 as the fastest shape: the slot is
+    // refilled as soon as it has been copied to registers, so 16 x 5 KB stay in flight
+    // per SM.  The diagnostic switches QG_GROUPED_CTAS_PER_SM (1 or 2) and
+    // QG_GROUPED_SLOTS (slots per warp) override it.
     int per_sm = env_int("QG_GROUPED_CTAS_PER_SM", 2);
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 2) per_sm = 2;
-    const int slot = (bits == 4 ? stream::Slot<4>::BYTES : stream::Slot<6>::BYTES) + 8;
+    const int slot = bits == 4 ? stream::Slot<4>::BYTES : stream::Slot<6>::BYTES;
     int D = env_int("QG_GROUPED_SLOTS", 1);
     if (D < 1) D = 1;
     if (D > 16) D = 16;
     const size_t cap = (size_t)lc.max_smem_optin - 1024;
-    while ((size_t)8 * D * slot > cap && D > 1) --D;
-    const size_t smem = (size_t)8 * D * slot;
+    while (stream::xq_offset(8 * D, slot) + (size_t)p.img_bytes > cap && D > 1) --D;
+    const size_t smem = stream::xq_offset(8 * D, slot) + (size_t)p.img_bytes;
     p.stages_per_warp = D;
-    const void* kern;
-    if (bits == 4)
-        kern = per_sm == 1 ? (const void*)grouped_gemv_kernel<4, 1> : (const void*)grouped_gemv_kernel<4, 2>;
-    else
-        kern = per_sm == 1 ? (const void*)grouped_gemv_kernel<6, 1> : (const void*)grouped_gemv_kernel<6, 2>;
-    if (int e = ensure_smem_attr(kern, smem, lc)) return e;
+    using K = void (*)(GParams);
+    static const K kerns[2][2][2] = {
+        {{grouped_gemv_kernel<4, 1, false>, grouped_gemv_kernel<4, 1, true>},
+         {grouped_gemv_kernel<4, 2, false>, grouped_gemv_kernel<4, 2, true>}},
+        {{grouped_gemv_kernel<6, 1, false>, grouped_gemv_kernel<6, 1, true>},
+         {grouped_gemv_kernel<6, 2, false>, grouped_gemv_kernel<6, 2, true>}}};
+    const K kern = kerns[bits == 4 ? 0 : 1][per_sm - 1][smx ? 1 : 0];
+    if (int e = ensure_smem_attr((const void*)kern, smem, lc)) return e;
     long long grid = (long long)lc.sm_count * per_sm;
     if (grid > units) grid = units;
     LaunchCtx lc2 = lc;
-    lc2.flags |= QG_FLAG_PDL;
-    const dim3 g3((unsigned)grid), b3(256);
-    if (bits == 4)
-        return per_sm == 1 ? launch_kernel(grouped_gemv_kernel<4, 1>, g3, b3, smem, lc2, p)
-                           : launch_kernel(grouped_gemv_kernel<4, 2>, g3, b3, smem, lc2, p);
-    return per_sm == 1 ? launch_kernel(grouped_gemv_kernel<6, 1>, g3, b3, smem, lc2, p)
-                       : launch_kernel(grouped_gemv_kernel<6, 2>, g3, b3, smem, lc2, p);
+    if (!smx) lc2.flags |= QG_FLAG_PDL;
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(256), smem, lc2, p);
 }
 
 }  // namespace qg

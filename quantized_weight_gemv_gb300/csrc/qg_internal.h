@@ -97,7 +97,9 @@ size_t mma_workspace_bytes(int k, int batch);
 // ws: the activation image (mma_workspace_bytes), or null to quantise in every CTA
 int launch_mma(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc);
 size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count);
-int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc);
+// fuse: allow the one-launch form (activations quantised in every CTA) when they are short
+int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc,
+                   bool fuse = false);
 size_t chain_workspace_bytes(const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase);
 // ws: the caller's chain workspace (control words first); arguments already validated
 int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase,

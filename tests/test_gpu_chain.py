@@ -1,7 +1,7 @@
 """GPU parity of the dependent GEMV chain (qgemv_chain) against the oracle's chain.
 
-Both launch modes are covered: the persistent cooperative kernel (default) and one
-grouped launch pair per phase (QG_FLAG_CHAIN_LAUNCHES)."""
+Both launch modes are covered: per-phase grouped launches (default) and the
+persistent cooperative kernel (QG_FLAG_CHAIN_PERSISTENT)."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +13,7 @@ from datagen import workloads as W
 from tests._gpu import DEV, assert_close, dev_w, oracle_gemv_par
 
 pytestmark = pytest.mark.gpu
-MODES = [0, qg.QG_FLAG_CHAIN_LAUNCHES]
+MODES = [0, qg.QG_FLAG_CHAIN_PERSISTENT]
 
 
 def _oracle_fn(w, x):
@@ -178,7 +178,7 @@ def test_decode_chain_modes_identical_and_equivariant(decode_chain):
     x0 = decode_chain[3]
     ch, ys, X = _decode_run(decode_chain, 0)
     base = [y.clone() for y in ys]
-    _, ys2, _ = _decode_run(decode_chain, qg.QG_FLAG_CHAIN_LAUNCHES)
+    _, ys2, _ = _decode_run(decode_chain, qg.QG_FLAG_CHAIN_PERSISTENT)
     for a, b in zip(base, ys2):
         assert torch.equal(a, b)
     for factor in (4.0, -1.0):
@@ -190,7 +190,7 @@ def test_decode_chain_modes_identical_and_equivariant(decode_chain):
 
 
 def test_chain_abort_word_stops_and_rearms():
-    """A set abort word makes every CTA stop at its next phase boundary without waiting
+    """Persistent kernel: a set abort word makes every CTA stop at its next phase boundary without waiting
     out the barrier; the workspace comes back zero and the next call is correct."""
     n = 2048
     ws_np = [datagen.make_quantized(4, 800 + i, n, n) for i in range(4)]
@@ -198,7 +198,7 @@ def test_chain_abort_word_stops_and_rearms():
     x0 = datagen.normal_f32(80, 1, n)
     X = torch.from_numpy(x0).to(DEV)
     ys = [torch.empty(n, device=DEV) for _ in range(4)]
-    ch = qg.ChainGemv(4, mats, [X, ys[0], ys[1], ys[2]], ys, [1, 1, 1, 1])
+    ch = qg.ChainGemv(4, mats, [X, ys[0], ys[1], ys[2]], ys, [1, 1, 1, 1], flags=qg.QG_FLAG_CHAIN_PERSISTENT)
     ctl = ch.ws[:qg.QG_CHAIN_CTL_BYTES].view(torch.int32)
     ctl[1] = 1
     torch.cuda.synchronize()

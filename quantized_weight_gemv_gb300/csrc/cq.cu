@@ -20,7 +20,7 @@ __device__ __forceinline__ void load_lane_group(const float* __restrict__ src, f
     if constexpr (J % 4 == 0) {
 #pragma unroll
         for (int q = 0; q < J / 4; ++q) {
-            const float4 t = __ldcg(reinterpret_cast<const float4*>(src) + q);  // may be a predecessor's output
+            const float4 t = reinterpret_cast<const float4*>(src)[q];
             v[4 * q] = t.x;
             v[4 * q + 1] = t.y;
             v[4 * q + 2] = t.z;
@@ -28,7 +28,7 @@ __device__ __forceinline__ void load_lane_group(const float* __restrict__ src, f
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < J; ++j) v[j] = __ldcg(src + j);
+        for (int j = 0; j < J; ++j) v[j] = src[j];
     }
 }
 

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) grouped_quantize_kernel(const __grid_cons
         const int nb = 1 << d.log2nb;
         float s;
         int S;
-        const int q = quantize_lane(__ldcg(d.x + 32 * b + lane), s, S);
+        const int q = quantize_lane(d.x[32 * b + lane], s, S);
         const XqView v = xq_view(p.ws + d.ws_off, nb);
         if (lane < 16)
             v.lo[16 * b + lane] = (int8_t)q;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
     unsigned char* const xbase = SMX ? smem + stream::xq_offset(8 * D, SL::BYTES) : p.ws;
     if constexpr (SMX) {
         for (int i = 0; i < p.nin; ++i)
-            quantize_x_cols<256, true>(p.in[i].x, p.in[i].k, 1, xbase + p.in[i].off, 0, threadIdx.x);
+            quantize_x_cols<256>(p.in[i].x, p.in[i].k, 1, xbase + p.in[i].off, 0, threadIdx.x);
         __syncthreads();
     }
 

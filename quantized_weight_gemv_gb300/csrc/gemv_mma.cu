@@ -125,11 +125,10 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
             const int c = idx_all / nf4;
             rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (idx_all < total && c < batch)
-                rv[i] = __ldcg(reinterpret_cast<const float4*>(X + (size_t)c * k) + (idx_all - c * nf4));
+                rv[i] = __ldg(reinterpret_cast<const float4*>(X + (size_t)c * k) + (idx_all - c * nf4));
         }
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
-            if (r0 + i * nthreads >= total) break;  // the same for every thread
             const int idx_all = r0 + i * nthreads + t;
             const int c = idx_all / nf4;
             const int idx = idx_all - c * nf4;

@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
     pdl_wait();  // x, y and the workspace may belong to the preceding kernel
     if (threadIdx.x == 0) pdl_launch_dependents();
 
-    quantize_x_cols<256, true>(p.x, p.k, p.batch, smem, xstride, threadIdx.x);
+    quantize_x_cols<256>(p.x, p.k, p.batch, smem, xstride, threadIdx.x);
     __syncthreads();
 
     float bv = __int_as_float(0x7fc00000);
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
          blk += (long long)gridDim.x * 8) {
         float s;
         int S;
-        const int q = quantize_lane(__ldcg(x + blk * 32 + lane), s, S);
+        const int q = quantize_lane(x[blk * 32 + lane], s, S);
         xq[blk * 32 + lane] = (int8_t)q;
         if (lane == 0) {
             xs[blk] = s;

@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
 
     // ---- activation prologue (after the preceding kernel, which may have written x)
     pdl_wait();
-    quantize_x_cols<256, true>(p.x, p.k, p.batch, xqbase, xstride, threadIdx.x);
+    quantize_x_cols<256>(p.x, p.k, p.batch, xqbase, xstride, threadIdx.x);
     __syncthreads();
 
     uint4 xl[BC][NXR], xh[BC][NXR];

@@ -117,8 +117,8 @@ __host__ __device__ constexpr int xq_bytes(int nb) { return 40 * nb; }
 // and sum need three shuffles.  All CHUNK loads of a round are issued before any is
 // used, so the prologue costs about one L2 round trip per CHUNK*NT float4s.
 // L2ONLY reads x with ld.global.cg: for a vector other SMs wrote during the same
-// launch, or that a preceding kernel wrote while this one had already started
-// (programmatic dependent launch), which the non-coherent (and L1) path may hold stale.
+// launch, which the non-coherent (and L1) path may hold stale.  (What a preceding
+// kernel wrote is visible to every read issued after griddepcontrol.wait.)
 template <int NT, bool L2ONLY = false>
 __device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int k, int batch, unsigned char* base,
                                                 int stride, int t) {

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ l
     const long long r0 = (long long)blockIdx.x * n / gridDim.x, r1 = (long long)(blockIdx.x + 1) * n / gridDim.x;
     float m = -INFINITY, s = 0.0f;
     for (long long i = r0 + threadIdx.x; i < r1; i += blockDim.x) {
-        const float v = __ldcg(logits + i);  // written by the preceding kernel
+        const float v = logits[i];
         if (v == v) lse_merge(m, s, v, 1.0f);
     }
     // best allowed (value, lowest id) over this CTA's share of the allowed list
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ l
     for (long long j = a0 + threadIdx.x; j < a1; j += blockDim.x) {
         const long long id = allowed ? (long long)allowed[j] : j;
         if (id < 0 || id >= n) continue;
-        const float v = __ldcg(logits + id);
+        const float v = logits[id];
         if (better(v, (int)id, bv, bi)) {
             bv = v;
             bi = (int)id;

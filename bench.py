@@ -60,6 +60,7 @@ CASES = {
     "q4_down_2048x16384": (4, 2048, 16384, 8),
     "q4_q_2048x2048": (4, 2048, 2048, 64),
     "q6_vocab_262144x2048": (6, 262144, 2048, 1),
+    "q2_vocab_262144x1536": (2, 262144, 1536, 2),
     "q4_batched_b4_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b8_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
@@ -110,7 +111,7 @@ def run_case(args):
     batch = int(args.case.split("_batched_b")[1].split("_")[0]) if "_batched_b" in args.case else 1
     x = torch.from_numpy(datagen.normal_f32(11, 1, batch * k).reshape(batch, k)).to(device)
     y = torch.empty(batch, n, device=device)
-    if bits == 6:
+    if bits in (2, 6):
         ws = qg.vocab_workspace(device)
         am = torch.empty(1, dtype=torch.int32, device=device)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -124,12 +125,12 @@ def run_case(args):
         elif bits == 4:
             qg.qgemv_q4(r["lo"], r["scale"], r["min"], x[0], y=y[0])
         else:
-            qg.vocab_softcap_argmax(6, r["lo"], r["hi"], r["scale"], r["min"], x[0], W.SOFTCAP, logits=y[0],
-                                    argmax=am, ws=ws)
+            qg.vocab_softcap_argmax(bits, r["lo"], r.get("hi"), r["scale"], r.get("min"), x[0], W.SOFTCAP,
+                                    logits=y[0], argmax=am, ws=ws)
     e1.record()
     torch.cuda.synchronize()
     calls = args.reps * copies
-    nbytes = (W.q4_bytes if bits == 4 else W.q6_bytes)(n, k)
+    nbytes = {2: W.q2_bytes, 4: W.q4_bytes, 6: W.q6_bytes}[bits](n, k)
     ms = e0.elapsed_time(e1) / calls
     print(json.dumps({"case": args.case, "batch": batch, "calls": calls, "us_per_call_eager": ms * 1e3,
                       "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
@@ -357,7 +358,38 @@ def extra_rows(device):
     nbytes = W.q6_bytes(W.VOCAB, W.HIDDEN)
     rows["vocab_q6_262144x2048_softcap_argmax"] = {"us_per_call": ms * 1e3, "GBps": nbytes / ms / 1e6,
                                                    "frac_of_8TBps": nbytes / ms / 1e6 / 8000.0}
+    # constrained selection over those logits (about 1 % of the ids allowed), alone and
+    # fused behind the projection
+    allowed = torch.from_numpy(W.select_allowed()).to(device)
+    tok = torch.empty(1, dtype=torch.int32, device=device)
+    lp = torch.empty(1, dtype=torch.float32, device=device)
+    sws = qg.select_workspace(device)
+    g = graph_of(lambda: [qg.qg_logits_select(logits, allowed, token=tok, logprob=lp, ws=sws, flags=qg.QG_FLAG_PDL)
+                          for _ in range(64)], st)
+    ms_sel = time_graph(g, st, 20) / 64
+    vws = qg.vocab_select_workspace(device)
+    g = graph_of(lambda: qg.vocab_softcap_select(6, w6d["lo"], w6d["hi"], w6d["scale"], w6d["min"], x6t, W.SOFTCAP,
+                                                 allowed=allowed, logits=logits, token=tok, logprob=lp, ws=vws), st)
+    ms_vsel = time_graph(g, st, 50)
+    rows["select_262144_logits_1pct_allowed"] = {
+        "us_per_call_l2_resident": ms_sel * 1e3, "allowed": int(allowed.numel()),
+        "vocab_q6_softcap_select_us": ms_vsel * 1e3, "vocab_q6_softcap_select_GBps": nbytes / ms_vsel / 1e6}
     del w6d, g, logits
+    torch.cuda.empty_cache()
+
+    # int2 LM head (zero point 2), 262144 x 1536: 126 MB, two rotating copies (> L2)
+    w2, x2 = W.vocab_q2()
+    w2d = qg.to_device(w2, device)
+    rot2 = [w2d, {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in w2d.items()}]
+    x2t = torch.from_numpy(x2).to(device)
+    logits2 = torch.empty(W.VOCAB, device=device)
+    g = graph_of(lambda: [qg.vocab_softcap_argmax(2, r["lo"], None, r["scale"], None, x2t, W.SOFTCAP, logits=logits2,
+                                                  argmax=am, ws=ws, flags=qg.QG_FLAG_PDL) for r in rot2], st)
+    ms2 = time_graph(g, st, 50) / 2
+    nb2 = W.q2_bytes(W.VOCAB, W.VOCAB_Q2_K)
+    rows["vocab_q2_262144x1536_softcap_argmax"] = {"us_per_call": ms2 * 1e3, "GBps": nb2 / ms2 / 1e6,
+                                                   "bytes": nb2}
+    del rot2, w2d, g, logits2
     torch.cuda.empty_cache()
 
     # small-batch MMVQ

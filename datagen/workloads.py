@@ -9,6 +9,8 @@ Shapes, distributions and seeds:
 * ``decode_chain`` - the same weights, each GEMV reading an earlier one's output
   (``decode_chain_plan``); one external x[2048] ~ N(0, 1).
 * ``vocab_q6``   - Q6 W 262144x2048 (N(0, 0.02)), x[2048] N(0, 1); soft-cap 30; seed 2.
+* ``vocab_q2``   - Q2 (zero point 2) W 262144x1536 (N(0, 0.02)), x[1536] N(0, 1); seed 5.
+* ``select_allowed`` - ~1 % of the vocabulary ids, uniform, distinct; seed 6.
 * ``batched_q4`` - Q4 W 16384x2048 (N(0, 0.02)); X[B][2048] N(0, 1), column b drawn
   from offset b*2048 of the activation stream; seed 3.
 * ``cq``         - K = 512 (one 512-value group); codebook 16 x f16 N(0, 0.05),
@@ -21,7 +23,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import STREAM_X, make_cq, make_quantized, normal_f32
+from . import STREAM_X, make_cq, make_quantized, normal_f32, uniform_f32
 
 HIDDEN = 2048
 FFN = 16384
@@ -53,6 +55,11 @@ def q4_bytes(n: int, k: int) -> int:
 def q6_bytes(n: int, k: int) -> int:
     """Packed Q6 bytes: 16 B lo + 8 B hi + 2 B scale + 2 B min per block of 32."""
     return n * (k // 32) * 28
+
+
+def q2_bytes(n: int, k: int) -> int:
+    """Packed Q2 bytes: 8 B codes + 2 B scale per block of 32 (no min plane)."""
+    return n * (k // 32) * 10
 
 
 def cq_bytes(n: int, k: int) -> int:
@@ -115,6 +122,24 @@ def vocab_q6():
     w = make_quantized(6, 2, VOCAB, HIDDEN)
     x = normal_f32(2, STREAM_X, HIDDEN)
     return w, x
+
+
+VOCAB_Q2_K = 1536  # the int2 LM head's width (Gemma WebGPU Engine, "Roadmap": 262,144 x 1536)
+
+
+def vocab_q2():
+    """The int2 (zero point 2) LM head: Q2 W 262144x1536 ~ N(0, 0.02), x[1536] ~ N(0, 1); seed 5."""
+    w = make_quantized(2, 5, VOCAB, VOCAB_Q2_K)
+    x = normal_f32(5, STREAM_X, VOCAB_Q2_K)
+    return w, x
+
+
+def select_allowed(n: int = VOCAB, frac: float = 0.01, seed: int = 6) -> np.ndarray:
+    """A constrained-decoding allowed list: distinct sorted int32 ids, about frac * n of
+    them, drawn uniformly (stream 2 of the seed)."""
+    m = max(1, int(n * frac))
+    ids = np.unique((uniform_f32(seed, 2, m) * n).astype(np.int64) % n)
+    return ids.astype(np.int32)
 
 
 def batched_q4_weights():

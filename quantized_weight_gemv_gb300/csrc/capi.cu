@@ -118,7 +118,7 @@ static int gemv_common(int bits, const uint8_t* lo, const uint8_t* hi, const uin
         if (rc != QG_ERR_UNSUPPORTED) return rc;
     }
     if (!(flags & QG_FLAG_PLAIN) && stream_supported(bits, n, k, batch, EPI_STORE)) {
-        StreamParams sp = {lo, hi, scale, min, n, k, batch, 0, 0, x, y, 0.0f, nullptr, nullptr, nullptr};
+        StreamParams sp = {lo, hi, scale, min, n, k, batch, 0, x, y, 0.0f, nullptr, nullptr, nullptr};
         rc = launch_stream(sp, bits, EPI_STORE, lc);
         if (rc != QG_ERR_UNSUPPORTED) return rc;
     }
@@ -222,7 +222,7 @@ int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const u
     if (rc != QG_OK) return rc;
     VocabWorkspace* w = reinterpret_cast<VocabWorkspace*>(ws);
     if (!(flags & QG_FLAG_PLAIN) && stream_supported(bits, n_vocab, k, 1, EPI_ARGMAX)) {
-        StreamParams sp = {lo, hi, scale, min, n_vocab, k, 1, 0, 0, x, logits, softcap, argmax, w, nullptr};
+        StreamParams sp = {lo, hi, scale, min, n_vocab, k, 1, 0, x, logits, softcap, argmax, w, nullptr};
         rc = launch_stream(sp, bits, EPI_ARGMAX, lc);
         if (rc != QG_ERR_UNSUPPORTED) return rc;
     }

@@ -5,7 +5,9 @@ namespace qg {
 
 bool stream_supported(int bits, int n, int k, int batch, int epi) {
     if (bits != 2 && bits != 4 && bits != 6) return false;
-    if (k < 256 || k > 16384 || (k & (k - 1)) != 0) return false;  // nb a power of two in [8, 512]
+    // nb = k/32 a power of two in [8, 512], or 48 (k = 1536, the hidden width of the
+    // int2 LM head of the Gemma WebGPU Engine, "Roadmap")
+    if (k != 1536 && (k < 256 || k > 16384 || (k & (k - 1)) != 0)) return false;
     if (batch < 1 || batch > 4) return false;
     if (epi == EPI_ARGMAX && batch != 1) return false;
     (void)n;
@@ -15,10 +17,6 @@ bool stream_supported(int bits, int n, int k, int batch, int epi) {
 int launch_stream(const StreamParams& p0, int bits, int epi, const LaunchCtx& lc) {
     if (!stream_supported(bits, p0.n, p0.k, p0.batch, epi)) return QG_ERR_UNSUPPORTED;
     StreamParams p = p0;
-    const int nb = p.k >> 5;
-    int l = 0;
-    while ((1 << l) < nb) ++l;
-    p.log2nb = l;
     if (bits == 2) return launch_stream_bits<2>(p, epi, lc);
     return bits == 4 ? launch_stream_bits<4>(p, epi, lc) : launch_stream_bits<6>(p, epi, lc);
 }

@@ -149,15 +149,24 @@ __device__ __forceinline__ void emit_row(const StreamParams& p, long long row, c
     }
 }
 
-template <int BITS, int BC, int EPI, int LOG2NB>
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }
+
+// NB = k / 32 blocks per row: a power of two from 8 to 512, or 48 (k = 1536).  For 48 a
+// stage holds 5 whole rows (240 blocks), the activation words come from shared memory
+// and each row is summed over the warp on its own (GEN below).
+template <int BITS, int BC, int EPI, int NB>
 __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(StreamParams p) {
     using SL = Slot<BITS>;
-    constexpr int NB = 1 << LOG2NB;
+    constexpr bool GEN = (NB & (NB - 1)) != 0;       // not a power of two
+    constexpr int LOG2NB = GEN ? 0 : ilog2(NB);
     constexpr int R = NB >= SBW ? 1 : SBW / NB;       // rows per stage
     constexpr int PARTS = NB > SBW ? NB / SBW : 1;    // stages per row
-    constexpr int NXB = NB >= 32 ? (NB < SBW ? NB / 32 : 8) : 1;  // distinct activation blocks per lane
+    // distinct activation blocks per lane.  GEN (48 blocks per row): lane l meets blocks
+    // (l + 32j) mod 48, and 96 = 0 mod 48, so only the three of j mod 3
+    constexpr int NXB = GEN ? 3 : NB >= 32 ? (NB < SBW ? NB / 32 : 8) : 1;
     constexpr bool XREG = NB <= 128 && BC * NXB <= 8;  // activation words in registers
     constexpr int NXR = XREG ? NXB : 1;
+    static_assert(!GEN || (NB % 16 == 0 && NB < SBW), "rows of a stage: 16-block multiples below 256");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     if constexpr (XREG) {
 #pragma unroll
         for (int j = 0; j < NXR; ++j) {
-            const int blk = NB >= 32 ? lane + 32 * j : (lane & (NB - 1));
+            const int blk = GEN ? (lane + 32 * j) % NB : NB >= 32 ? lane + 32 * j : (lane & (NB - 1));
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
                 const XqView v = xq_view(xqbase + c * xstride, NB);
@@ -275,7 +284,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         float pj[BC][JPL];
 #pragma unroll
         for (int j = 0; j < JPL; ++j) {
-            const int rloc = (NB >= SBW) ? 0 : ((lane + 32 * j) >> LOG2NB);
+            const int rloc = (NB >= SBW) ? 0 : GEN ? (lane + 32 * j) / NB : ((lane + 32 * j) >> LOG2NB);
 
             const float d = half_bits_to_float(dh[j]);
             const float m = BITS == 2 ? -2.0f * d : half_bits_to_float(mh[j]);  // Q2: zero point 2
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
                     const int xj = NB >= 32 ? (j % NXR) : 0;
                     r = block_combine(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), d, m, xs[c][xj], xS[c][xj]);
                 } else {
-                    const int blk = (part * SBW + lane + 32 * j) & (NB - 1);
+                    const int blk = GEN ? (lane + 32 * j) % NB : (part * SBW + lane + 32 * j) & (NB - 1);
                     const XqView v = xq_view(xqbase + c * xstride, NB);
                     const uint4 a = *reinterpret_cast<const uint4*>(v.lo + 16 * blk);
                     const uint4 b = *reinterpret_cast<const uint4*>(v.hi + 16 * blk);
@@ -297,7 +306,34 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
             }
         }
 
-        if constexpr (NB >= 32) {
+        if constexpr (GEN) {
+            // rows straddle the lanes' block groups: each lane sums its blocks per row, the
+            // R rows padded to 8 go through one halving tree (lane l ends with row l / 4)
+#pragma unroll
+            for (int c = 0; c < BC; ++c) {
+                float rs[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    float s = 0.0f;
+                    if (r < R) {
+#pragma unroll
+                        for (int j = 0; j < JPL; ++j) s += (lane + 32 * j) / NB == r ? pj[c][j] : 0.0f;
+                    }
+                    rs[r] = s;
+                }
+                halving_reduce<8, 5>(rs);
+                pj[c][0] = rs[0];
+            }
+            if ((lane & 3) == 0) {
+                const int r = lane >> 2;
+                if (r < rows_u) {
+                    float out[BC];
+#pragma unroll
+                    for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
+                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+                }
+            }
+        } else if constexpr (NB >= 32) {
             // R rows per stage, JPL/R consecutive j per row
             constexpr int JR = JPL / R;
 #pragma unroll

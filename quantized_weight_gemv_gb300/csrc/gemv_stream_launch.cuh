@@ -14,11 +14,10 @@ inline int env_int(const char* name, int dflt) {
     return atoi(v);
 }
 
-template <int BITS, int BC, int EPI, int L>
+template <int BITS, int BC, int EPI, int NB>
 int launch_t(StreamParams p, const LaunchCtx& lc) {
     using SL = Slot<BITS>;
-    auto kern = gemv_stream_kernel<BITS, BC, EPI, L>;
-    constexpr int NB = 1 << L;
+    auto kern = gemv_stream_kernel<BITS, BC, EPI, NB>;
     constexpr int W = 8;  // warps per CTA
     const size_t fixed = (size_t)BC * xq_stride(NB);
     // Default: one ring slot per warp and two CTAs per SM (measured on GB300 as the
@@ -48,14 +47,15 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
 
 template <int BITS, int BC, int EPI>
 int launch_l(const StreamParams& p, const LaunchCtx& lc) {
-    switch (p.log2nb) {
-        case 3: return launch_t<BITS, BC, EPI, 3>(p, lc);
-        case 4: return launch_t<BITS, BC, EPI, 4>(p, lc);
-        case 5: return launch_t<BITS, BC, EPI, 5>(p, lc);
-        case 6: return launch_t<BITS, BC, EPI, 6>(p, lc);
-        case 7: return launch_t<BITS, BC, EPI, 7>(p, lc);
+    switch (p.k >> 5) {
         case 8: return launch_t<BITS, BC, EPI, 8>(p, lc);
-        case 9: return launch_t<BITS, BC, EPI, 9>(p, lc);
+        case 16: return launch_t<BITS, BC, EPI, 16>(p, lc);
+        case 32: return launch_t<BITS, BC, EPI, 32>(p, lc);
+        case 48: return launch_t<BITS, BC, EPI, 48>(p, lc);
+        case 64: return launch_t<BITS, BC, EPI, 64>(p, lc);
+        case 128: return launch_t<BITS, BC, EPI, 128>(p, lc);
+        case 256: return launch_t<BITS, BC, EPI, 256>(p, lc);
+        case 512: return launch_t<BITS, BC, EPI, 512>(p, lc);
     }
     return QG_ERR_UNSUPPORTED;
 }

@@ -32,7 +32,6 @@ struct StreamParams {
     const uint16_t* scale;
     const uint16_t* min;
     int n, k, batch;
-    int log2nb;  // log2(k/32)
     int stages;  // ring depth
     const float* x;
     float* y;

@@ -87,7 +87,7 @@ def test_blockdots_extremes_bit_exact():
 
 # ---------------------------------------------------------------- GEMV
 SHAPES = [(1, 32), (7, 96), (33, 256), (100, 512), (1000, 1024), (1024, 1024), (333, 2048), (2049, 2048),
-          (77, 4096), (19, 8192), (40, 16384), (3, 1056), (5, 32768)]
+          (77, 4096), (19, 8192), (40, 16384), (3, 1056), (5, 32768), (1, 1536), (4, 1536), (1234, 1536)]
 
 
 @pytest.mark.parametrize("bits", [2, 4, 6])
@@ -166,8 +166,9 @@ def test_gemv_empty_is_noop():
 @pytest.mark.parametrize("bits", [2, 4, 6])
 @pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 16])
 @pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
-def test_batched(bits, batch, flags):
-    n, k = 1000, 2048
+@pytest.mark.parametrize("k", [2048, 1536])
+def test_batched(bits, batch, flags, k):
+    n = 1000
     w = datagen.make_quantized(bits, 300 + batch, n, k)
     X = datagen.normal_f32(300 + batch, 1, batch * k).reshape(batch, k)
     wd = dev_w(w)
@@ -213,7 +214,7 @@ def _vocab_check(w, x, softcap, flags=0, ws=None):
 
 
 @pytest.mark.parametrize("bits", [2, 4, 6])
-@pytest.mark.parametrize("n,k", [(1, 32), (1000, 256), (5000, 2048), (3001, 1056), (700, 16384)])
+@pytest.mark.parametrize("n,k", [(1, 32), (1000, 256), (5000, 2048), (3001, 1056), (700, 16384), (4099, 1536)])
 @pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
 def test_vocab_random(bits, n, k, flags):
     w = datagen.make_quantized(bits, n + 3 * k, n, k)
@@ -519,3 +520,11 @@ def test_int8_decisions_every_kernel(k):
     for name, ys in got.items():
         for b, yv in enumerate(ys):
             assert np.array_equal(yv.cpu().numpy().view(np.uint32), want[b].view(np.uint32)), (name, b)
+
+
+def test_int2_vocab_head_pages_shape():
+    """The int2 LM head at the pages' shape (262144 x 1536, Gemma WebGPU Engine "Roadmap")."""
+    n, k = 262144, 1536
+    w = datagen.make_quantized(2, 97, n, k)
+    x = datagen.normal_f32(97, 1, k)
+    _vocab_check(w, x, 30.0)

@@ -279,6 +279,7 @@ double or_logsumexp(const double* v, int64_t n) {
     for (int64_t i = 0; i < n; ++i)
         if (!isnan(v[i]) && v[i] > m) m = v[i];
     if (m == -INFINITY) return -INFINITY;
+    if (m == INFINITY) return INFINITY; /* exp(+inf) dominates the sum */
     double s = 0.0;
     for (int64_t i = 0; i < n; ++i)
         if (!isnan(v[i])) s += exp(v[i] - m);

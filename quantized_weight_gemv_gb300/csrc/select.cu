@@ -14,6 +14,11 @@ namespace qg {
 
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
     if (m2 == -INFINITY) return;
+    if (m == INFINITY || m2 == INFINITY) {  // an infinite term: log-sum-exp = +inf
+        m = INFINITY;
+        s = 1.0f;
+        return;
+    }
     if (m == -INFINITY) {
         m = m2;
         s = s2;
@@ -67,9 +72,26 @@ __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ l
     // log-sum-exp over this CTA's rows (NaN skipped)
     const long long r0 = (long long)blockIdx.x * n / gridDim.x, r1 = (long long)(blockIdx.x + 1) * n / gridDim.x;
     float m = -INFINITY, s = 0.0f;
-    for (long long i = r0 + threadIdx.x; i < r1; i += blockDim.x) {
-        const float v = logits[i];
-        if (v == v) lse_merge(m, s, v, 1.0f);
+    // four logits per step: their max first, then four independent exponentials
+    for (long long i0 = r0 + threadIdx.x; i0 < r1; i0 += 4 * (long long)blockDim.x) {
+        float v[4];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const long long i = i0 + (long long)q * blockDim.x;
+            v[q] = i < r1 ? logits[i] : __int_as_float(0x7fc00000);
+            if (v[q] == v[q]) cm = fmaxf(cm, v[q]);
+        }
+        if (cm == -INFINITY) continue;  // only NaN and -inf: no term
+        if (cm == INFINITY) {
+            lse_merge(m, s, INFINITY, 1.0f);
+            continue;
+        }
+        float cs = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (v[q] == v[q]) cs += expf(v[q] - cm);
+        lse_merge(m, s, cm, cs);
     }
     // best allowed (value, lowest id) over this CTA's share of the allowed list
     float bv = __int_as_float(0x7fc00000);
@@ -119,8 +141,8 @@ __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ l
 
 int launch_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token, float* logprob,
                   SelectWorkspace* ws, const LaunchCtx& lc) {
-    long long grid = ((long long)n + 8191) / 8192;
-    if (grid > lc.sm_count) grid = lc.sm_count;
+    long long grid = ((long long)n + 1023) / 1024;
+    if (grid > 2LL * lc.sm_count) grid = 2LL * lc.sm_count;
     if (grid > SELECT_MAX_CTAS) grid = SELECT_MAX_CTAS;
     if (grid < 1) grid = 1;
     return launch_kernel(select_kernel, dim3((unsigned)grid), dim3(256), 0, lc, logits, n, allowed, n_allowed, token,

@@ -528,3 +528,21 @@ def test_int2_vocab_head_pages_shape():
     w = datagen.make_quantized(2, 97, n, k)
     x = datagen.normal_f32(97, 1, k)
     _vocab_check(w, x, 30.0)
+
+
+def test_logits_select_infinities():
+    """An infinite logit: the log-sum-exp is +inf, the selected id is the +inf one when it
+    is allowed (log-probability inf - inf = NaN on both sides); -inf logits are never
+    better than finite ones and add nothing to the sum."""
+    n = 5000
+    v = datagen.normal_f32(77, 1, n)
+    v[100] = -np.inf
+    v[4000] = np.inf
+    t = torch.from_numpy(v).to(DEV)
+    for allowed in (None, np.array([5, 100, 4000], np.int32), np.array([5, 100], np.int32)):
+        a = None if allowed is None else torch.from_numpy(allowed).to(DEV)
+        tok, lp = qg.qg_logits_select(t, a)
+        ref_tok, ref_lp = oracle.select(v.astype(np.float64), allowed)
+        assert int(tok.item()) == ref_tok
+        got = float(lp.item())
+        assert (np.isnan(got) and np.isnan(ref_lp)) or got == ref_lp == -np.inf or abs(got - ref_lp) < 1e-9, (got, ref_lp)

@@ -557,3 +557,15 @@ def test_decode_chain_plan_shapes():
     # a link reads only outputs of earlier stages
     first = np.repeat(np.cumsum([0] + stages[:-1]), stages)
     assert all(sj < first[j] for j, sj in enumerate(src))
+
+
+def test_logsumexp_infinities_match_scipy():
+    """log sum exp with infinite terms: +inf if any term is +inf, -inf if all are -inf,
+    -inf terms contribute nothing (scipy.special.logsumexp fixes these values)."""
+    from scipy.special import logsumexp as sp_lse
+
+    cases = [[np.inf, 1.0, -2.0], [-np.inf, -np.inf], [-np.inf, 0.5, 3.0], [np.inf, np.inf]]
+    for c in cases:
+        assert oracle.logsumexp(np.array(c)) == sp_lse(np.array(c)), c
+    # NaN skipped, the rest as scipy
+    assert oracle.logsumexp(np.array([np.nan, 1.0, 2.0])) == pytest.approx(sp_lse([1.0, 2.0]), rel=1e-15)

@@ -79,8 +79,9 @@ int qg_version(void);
 /*
  * Device-side error word.  Kernels that wait on an mbarrier or on the other CTAs
  * give up after a bounded time and record a nonzero code here instead of hanging:
- * 1 a weight tile never landed, 4 a copy in flight never landed while stopping,
- * 8 a grid-wide barrier of qgemv_chain ran out.  Reads and clears the word of the
+ * 1 a weight tile never landed, 2 a ring slot was never freed (qgemv_chain's
+ * producer), 4 a copy in flight never landed while stopping, 8 a grid-wide barrier
+ * of qgemv_chain ran out.  Reads and clears the word of the
  * current device; synchronises the device.
  * Returns QG_OK or QG_ERR_CUDA; *code receives the word (0 = no error).
  */
@@ -178,8 +179,8 @@ int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const u
  * qg_logits_select: over logits l[n] (device fp32),
  *   token   = the allowed ID of the largest logit, the lowest ID among equal maxima,
  *             NaN never selected; -1 if no allowed ID qualifies;
- *   logprob = l[token] - log(sum_i exp(l[i])) over ALL n logits (NaN skipped);
- *             NaN when token is -1.
+ *   logprob = l[token] - log(sum_i exp(l[i])) over ALL n logits (NaN skipped; a
+ *             +inf logit makes the log-sum-exp +inf); NaN when token is -1.
  *   allowed : device int32 [n_allowed] token IDs in any order (ascending as the page
  *             has it; duplicates and IDs outside [0, n) are ignored), or NULL for all.
  *   token : device int32 [1];  logprob : device fp32 [1] (written).
@@ -258,8 +259,8 @@ int qgemv_grouped_noalloc(int bits, const qg_gemv_desc* descs, int count, unsign
  * (x) any vector written by an earlier phase or present before the call; the GEMVs
  * of one phase are independent of each other.  Each descriptor computes
  * y = GEMV(weights, x) exactly as qgemv_q4/qgemv_q6 define it, on x as the earlier
- * phases left it.  (Gemma WebGPU Engine, "Decode pipeline": a token's projections
- * run layer after layer, each on what the previous one wrote; genie-ai-runtime, "The
+ * phases left it.  (Gemma WebGPU Engine, "Roadmap": a layer's ordered dispatches,
+ * each projection reading the buffer the previous one wrote; genie-ai-runtime, "The
  * decode arc": the activation is quantised per matmul.)
  *   bits  : 4 (hi NULL) or 6
  *   descs : HOST array of `count` descriptors, read during the call only; n >= 0 and

@@ -183,8 +183,9 @@ def gemv_chain(mats, src, inputs, gemv_fn=None):
 
     Decode runs its projections back to back: what one matrix-vector product writes
     is the vector the next one quantises and reads (genie-ai-runtime, "The decode
-    arc": the activation is quantised per matmul; Gemma WebGPU Engine, "Decode
-    pipeline": layer after layer within one token).  GEMV j reads
+    arc": the activation is quantised per matmul; Gemma WebGPU Engine, "Roadmap":
+    a layer's ordered dispatches, each reading the buffer the previous one wrote).
+    GEMV j reads
       src[j] >= 0 : the output of GEMV src[j] (src[j] < j), handed over as the fp32
                     vector a kernel writes, i.e. the fp64 result rounded to fp32;
       src[j] <  0 : the external fp32 vector inputs[-src[j] - 1].

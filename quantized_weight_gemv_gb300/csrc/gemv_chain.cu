@@ -2,8 +2,10 @@
 // earlier phases wrote, in one persistent cooperative launch.
 //
 // A decode token is a chain: every projection quantises and reads a vector that an
-// earlier projection has just written (Gemma WebGPU Engine, "Decode pipeline";
-// genie-ai-runtime, "The decode arc": activation quantised per matmul).  One launch
+// earlier projection has just written (Gemma WebGPU Engine, "Roadmap": the layer's
+// ordered dispatches, the attention output bound straight into the O projection and
+// its output into the MLP; genie-ai-runtime, "The decode arc": activation quantised
+// per matmul, and "v1.2.0": ~448 dependent kernel launches per token).  One launch
 // per link pays a kernel boundary per link.  Here one CTA per SM walks all phases:
 //  * A phase is a list of GEMV descriptors whose inputs all exist before it.  Its work
 //    is cut as in the grouped GEMV: units of 256 blocks of 32 (whole rows), or single

@@ -127,6 +127,13 @@ __device__ __forceinline__ void halving_reduce(float (&v)[V]) {
     for (; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
 }
 
+// Row (within a 240-block stage of 48-block rows) of lane l's block l + 32j: lanes
+// 0-15 meet rows 0,0,1,2,2,3,4,4 and lanes 16-31 rows 0,1,1,2,3,3,4,5 (5: past the
+// stage).
+__device__ __forceinline__ int row48(int j, int lane) {
+    return lane < 16 ? (0x44322100 >> (4 * j)) & 15 : (0x54332110 >> (4 * j)) & 15;
+}
+
 // byte offset of the activation columns after `nslots` slots and their mbarriers
 __host__ __device__ constexpr size_t xq_offset(int nslots, int slot_bytes) {
     return (((size_t)nslots * (size_t)(slot_bytes + 8)) + 15) & ~(size_t)15;
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     constexpr int NXB = GEN ? 3 : NB >= 32 ? (NB < SBW ? NB / 32 : 8) : 1;
     constexpr bool XREG = NB <= 128 && BC * NXB <= 8;  // activation words in registers
     constexpr int NXR = XREG ? NXB : 1;
-    static_assert(!GEN || (NB % 16 == 0 && NB < SBW), "rows of a stage: 16-block multiples below 256");
+    static_assert(!GEN || NB == 48, "blocks per row: a power of two, or 48");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -284,7 +291,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         float pj[BC][JPL];
 #pragma unroll
         for (int j = 0; j < JPL; ++j) {
-            const int rloc = (NB >= SBW) ? 0 : GEN ? (lane + 32 * j) / NB : ((lane + 32 * j) >> LOG2NB);
+            const int rloc = (NB >= SBW) ? 0 : GEN ? row48(j, lane) : ((lane + 32 * j) >> LOG2NB);
 
             const float d = half_bits_to_float(dh[j]);
             const float m = BITS == 2 ? -2.0f * d : half_bits_to_float(mh[j]);  // Q2: zero point 2
@@ -307,20 +314,19 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         }
 
         if constexpr (GEN) {
-            // rows straddle the lanes' block groups: each lane sums its blocks per row, the
-            // R rows padded to 8 go through one halving tree (lane l ends with row l / 4)
+            // rows straddle the lanes' block groups (row48): each lane sums its blocks per
+            // row, the 5 rows padded to 8 go through one halving tree (lane l ends with row
+            // l / 4); pj of a block outside the stage's rows is already 0
+            const bool lo = lane < 16;
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
                 float rs[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    float s = 0.0f;
-                    if (r < R) {
-#pragma unroll
-                        for (int j = 0; j < JPL; ++j) s += (lane + 32 * j) / NB == r ? pj[c][j] : 0.0f;
-                    }
-                    rs[r] = s;
-                }
+                rs[0] = pj[c][0] + (lo ? pj[c][1] : 0.0f);
+                rs[1] = (lo ? 0.0f : pj[c][1]) + pj[c][2];
+                rs[2] = pj[c][3] + (lo ? pj[c][4] : 0.0f);
+                rs[3] = (lo ? 0.0f : pj[c][4]) + pj[c][5];
+                rs[4] = pj[c][6] + (lo ? pj[c][7] : 0.0f);
+                rs[5] = rs[6] = rs[7] = 0.0f;
                 halving_reduce<8, 5>(rs);
                 pj[c][0] = rs[0];
             }

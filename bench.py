@@ -237,21 +237,30 @@ def graph_of(fn, stream):
     return g
 
 
-def time_graph(g, stream, reps, warm=2):
+def time_graph_stats(g, stream, reps, warm=2, repeats=20):
+    """(median, p95) over `repeats` of the device time per replay (ms), each repeat
+    timing `reps` back-to-back replays with CUDA events on `stream`."""
     import torch
 
-    for _ in range(warm):
-        g.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
+        for _ in range(warm):
             g.replay()
-        e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps  # ms
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(repeats)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    t = np.sort(np.array([e0.elapsed_time(e1) / reps for e0, e1 in ev]))
+    return float(np.median(t)), float(t[min(len(t) - 1, int(np.ceil(0.95 * len(t))) - 1)])
+
+
+def time_graph(g, stream, reps, warm=2, repeats=20):
+    """Median device time per replay (ms) over `repeats` repeats of `reps` replays."""
+    return time_graph_stats(g, stream, reps, warm, repeats)[0]
 
 
 def time_eager(fn, stream, reps, warm=3):
@@ -420,16 +429,42 @@ def extra_rows(device):
         g = graph_of(lambda: [qg.cq_fwht_matvec(m["idx"], m["codebook"], m["row_scale"], xc, W.CQ_GROUP, y=yc,
                                                 flags=qg.QG_FLAG_PDL) for _ in range(64)], st)
         ms = time_graph(g, st, 20) / 64
-        rows[f"cq_{n}x512"] = {"us_per_call_l2_resident": ms * 1e3, "GBps": W.cq_bytes(n, W.CQ_K) / ms / 1e6}
-        del g
+        copies = 64 if n >= 8192 else 512  # > L2 (~134 MB)
+        rot = [m] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in m.items()}
+                     for _ in range(copies - 1)]
+        g2 = graph_of(lambda: [qg.cq_fwht_matvec(r["idx"], r["codebook"], r["row_scale"], xc, W.CQ_GROUP, y=yc,
+                                                 flags=qg.QG_FLAG_PDL) for r in rot], st)
+        ms2 = time_graph(g2, st, 5) / copies
+        nb = W.cq_bytes(n, W.CQ_K)
+        rows[f"cq_{n}x512"] = {"us_per_call_l2_resident": ms * 1e3, "GBps": nb / ms / 1e6,
+                               f"rotation_{copies}_copies_us_per_call": ms2 * 1e3,
+                               f"rotation_{copies}_copies_GBps": nb / ms2 / 1e6}
+        del g, g2, rot
     return rows
 
 
-def cpu_baseline(budget_s):
-    """The oracle, as it stands, on a bounded sample of the decode stream (single host thread)."""
+def host_cores() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def oracle_rows_threaded(w, x, row0, nrows, cores):
+    """The oracle's GEMV over rows [row0, row0 + nrows), the rows split over `cores` host
+    threads (each a plain oracle call on its slice; the C calls release the GIL)."""
+    import concurrent.futures as cf
+
     import oracle
+
+    bounds = [row0 + nrows * t // cores for t in range(cores + 1)]
+    with cf.ThreadPoolExecutor(cores) as ex:
+        list(ex.map(lambda t: oracle.gemv(w, x, bounds[t], bounds[t + 1] - bounds[t]), range(cores)))
+
+
+def cpu_baseline(budget_s):
+    """The oracle, as it stands, on a bounded sample of the decode stream, every host core
+    working on a slice of each GEMV's rows."""
     from datagen import workloads as W
 
+    cores = host_cores()
     done_bytes = 0
     done_gemv = 0
     t_total = 0.0
@@ -439,7 +474,7 @@ def cpu_baseline(budget_s):
         for proj in range(7):
             w, x = W.decode_projection(layer, proj)
             t0 = time.perf_counter()
-            oracle.gemv(w, x)
+            oracle_rows_threaded(w, x, 0, w["n"], cores)
             t_total += time.perf_counter() - t0
             done_bytes += W.q4_bytes(*W.PROJ_SHAPES[proj])
             done_gemv += 1
@@ -447,9 +482,10 @@ def cpu_baseline(budget_s):
                 break
         sample.append(layer)
         layer += 1
-    return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{done_gemv} full GEMVs of decode layers {sample[0]}..{sample[-1]} "
-                      f"({done_bytes / 1e6:.0f} MB of packed weights, fp64 scalar C, one thread)",
+                      f"({done_bytes / 1e6:.0f} MB of packed weights, fp64 scalar C, rows split over "
+                      f"{cores} host threads)",
             "seconds": t_total, "gemv_per_s": done_gemv / t_total}
 
 
@@ -462,18 +498,21 @@ def run_reference(args, ws, rank):
     from datagen import workloads as W
 
     oracle.build()
-    # one step = a bounded sample of the decode stream: 256 rows of one projection of
-    # layer 0, cycling through the seven projections and their row ranges, so that
-    # --steps K --warmup W ends within minutes
+    cores = host_cores()
+    # one step = a bounded sample of the decode stream: 256 rows per host core of one
+    # projection of layer 0, cycling through the seven projections and their row ranges,
+    # so that --steps K --warmup W ends within minutes
     layer0 = [W.decode_projection(0, proj) for proj in range(7)]
-    rows_per_step = 256
+    rows_per_step = 256 * cores
 
     def step(i):
         proj = i % 7
         w, x = layer0[proj]
-        row0 = ((i // 7) * rows_per_step) % w["n"]
-        oracle.gemv(w, x, row0, rows_per_step)
-        return W.q4_bytes(rows_per_step, w["k"])
+        rows = min(rows_per_step, w["n"])
+        row0 = ((i // 7) * rows) % w["n"]
+        rows = min(rows, w["n"] - row0)
+        oracle_rows_threaded(w, x, row0, rows, cores)
+        return W.q4_bytes(rows, w["k"])
 
     for i in range(args.warmup):
         step(i)
@@ -489,10 +528,10 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "decode_layers (35 layers x 7 Q4 projections, hidden 2048, FFN 16384); "
-                               "per step a 256-row slice of one layer-0 projection, cycling",
-                   "oracle": "fp64 scalar C, one host thread"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "per step: 256 rows of one of the 7 layer-0 projections, cycling"},
+                               f"per step a {rows_per_step}-row slice of one layer-0 projection, cycling",
+                   "oracle": f"fp64 scalar C, rows split over {cores} host threads"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {rows_per_step} rows of one of the 7 layer-0 projections, cycling"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
@@ -575,6 +614,9 @@ def run_ours(args, ws, rank, local):
         ms_total = float(tt.item())
     ms_step = ms_total / args.steps
     value = ws * total_bytes / (ms_step * 1e-3) / 1e9  # GB/s, all ranks
+    med, p95 = time_graph_stats(g, stream, 50, warm=2, repeats=20)
+    step_stats = {"median_ms": med, "p95_ms": p95, "repeats": 20, "replays_per_repeat": 50,
+                  "median_GBps": total_bytes / (med * 1e-3) / 1e9}
 
     # ---- end to end through the public API with host buffers: every step copies its
     # activations from pinned host memory, runs the 245 calls (replayed graph of the
@@ -696,6 +738,7 @@ def run_ours(args, ws, rank, local):
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
+        "ms_per_step_stats": step_stats,
         "other_launch_mode": other_mode,
         "decode_chain": chain,
         "clocks": clocks,

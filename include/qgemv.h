@@ -4,9 +4,11 @@
  * The library computes the decode-time matrix-vector product against
  * block-quantised weights: y = W_deq x with the activation x quantised to int8
  * per block of 32 and the weights stored as 4-bit or 6-bit codes with an fp16
- * scale and min per block of 32 (w = scale * code + min).  Its neighbours are a
- * small-batch variant, a Walsh-Hadamard + codebook (CQ) matvec, and a
- * vocabulary projection finished with logit soft-capping and argmax.
+ * scale and min per block of 32 (w = scale * code + min), or as 2-bit codes with
+ * an fp16 scale and zero point 2 (w = scale * (code - 2)).  Its neighbours are a
+ * small-batch variant, a Walsh-Hadamard + codebook (CQ) matvec, a vocabulary
+ * projection finished with logit soft-capping and argmax, constrained token
+ * selection, a grouped multi-matrix dispatch and a dependent GEMV chain.
  *
  * Conventions for every call:
  *  - Pointers named as device buffers are CUDA device pointers owned by the
@@ -50,7 +52,7 @@ enum qg_status {
     QG_OK = 0,
     QG_ERR_INVALID_ARG = -1, /* null pointer, size out of range, k not a multiple of 32, ... */
     QG_ERR_ALIGNMENT = -2,   /* a buffer that must start on a 16-byte boundary does not */
-    QG_ERR_UNSUPPORTED = -3, /* bits other than 4/6, group size not supported, shape too large */
+    QG_ERR_UNSUPPORTED = -3, /* bits not supported by the call, group size not supported, shape too large */
     QG_ERR_WORKSPACE = -4,   /* workspace missing or smaller than the reported size */
     QG_ERR_CUDA = -5         /* the CUDA launch itself failed */
 };

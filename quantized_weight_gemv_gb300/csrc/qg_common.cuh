@@ -173,53 +173,9 @@ __device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int
     }
 }
 
-// ---------------------------------------------------------------- unpack + dp4a block dot
+// ---------------------------------------------------------------- dp4a block dots
 // 16 code bytes of a Q4 block: word w (bytes 4w..4w+3) carries codes 4w..4w+3 in its
 // low nibbles and codes 16+4w..16+4w+3 in its high nibbles.
-struct Codes32 {
-    uint32_t lo[4];  // codes 0..15, one per byte
-    uint32_t hi[4];  // codes 16..31
-};
-
-__device__ __forceinline__ Codes32 unpack_q4(uint4 c) {
-    Codes32 r;
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        r.lo[i] = w[i] & 0x0F0F0F0Fu;
-        r.hi[i] = (w[i] >> 4) & 0x0F0F0F0Fu;
-    }
-    return r;
-}
-
-// Q6: the 8 hi bytes hold the top two bits of codes t, t+8, t+16, t+24 in byte t.
-// Codes 4w..4w+3 sit in bytes 4(w&1).. of word h[w&1] at bit pair w>>1; codes
-// 16+4w.. at bit pair 2 + (w>>1).
-__device__ __forceinline__ Codes32 unpack_q6(uint4 c, uint2 h) {
-    Codes32 r = unpack_q4(c);
-    const uint32_t hw[2] = {h.x, h.y};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t src = hw[i & 1];
-        r.lo[i] |= ((src >> (2 * (i >> 1))) & 0x03030303u) << 4;
-        r.hi[i] |= ((src >> (4 + 2 * (i >> 1))) & 0x03030303u) << 4;
-    }
-    return r;
-}
-
-// sum over the 32 codes of code * xq (codes 0..63 are non-negative in a signed byte);
-// two independent dp4a chains
-__device__ __forceinline__ int block_dot(const Codes32& c, uint4 xlo, uint4 xhi) {
-    int a = __dp4a((int)c.lo[0], (int)xlo.x, 0);
-    int b = __dp4a((int)c.hi[0], (int)xhi.x, 0);
-    a = __dp4a((int)c.lo[1], (int)xlo.y, a);
-    b = __dp4a((int)c.hi[1], (int)xhi.y, b);
-    a = __dp4a((int)c.lo[2], (int)xlo.z, a);
-    b = __dp4a((int)c.hi[2], (int)xhi.z, b);
-    a = __dp4a((int)c.lo[3], (int)xlo.w, a);
-    b = __dp4a((int)c.hi[3], (int)xhi.w, b);
-    return a + b;
-}
 
 // dp4a with unsigned bytes in a and signed bytes in b
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -271,7 +227,10 @@ __device__ __forceinline__ int qdot(uint4 cw, uint2 hw, uint4 xlo, uint4 xhi) {
         (void)hw;
         return block_dot_q4(cw, xlo, xhi);
     } else {
-        return block_dot(unpack_q6(cw, hw), xlo, xhi);
+        // Q6 = low nibbles (the Q4 plane) + 16 x the high bit pairs (the Q2 plane layout):
+        // by linearity the dot is the Q4 dot of the low plane plus 16 x the Q2 dot of the
+        // high plane, exact in int32
+        return block_dot_q4(cw, xlo, xhi) + (block_dot_q2(hw, xlo, xhi) << 4);
     }
 }
 

@@ -210,3 +210,53 @@ def test_chain_abort_word_stops_and_rearms():
     refs = oracle.gemv_chain(ws_np, [-1, 0, 1, 2], [x0])
     for y, r in zip(ys, refs):
         assert_close(y.cpu().numpy().astype(np.float64), r)
+
+
+@pytest.mark.parametrize("flags", MODES)
+def test_chain_empty_descriptors_and_phases(flags):
+    """Descriptors with n = 0 are skipped, and a phase made only of them adds no boundary."""
+    n, k = 1024, 1024
+    ws_np = [datagen.make_quantized(4, 900 + i, n, k) for i in range(3)]
+    mats = [dev_w(w) for w in ws_np]
+    empty = dict(mats[0])
+    empty["lo"] = mats[0]["lo"][:0]
+    empty["scale"] = mats[0]["scale"][:0]
+    empty["min"] = mats[0]["min"][:0]
+    empty["n"] = 0
+    x0 = datagen.normal_f32(91, 1, k)
+    X = torch.from_numpy(x0).to(DEV)
+    ys = [torch.full((n,), float("nan"), device=DEV) for _ in range(3)]
+    ye = [torch.empty(0, device=DEV) for _ in range(3)]
+    # phases: [g0, empty] [empty] [g1, empty] [g2]
+    descs = [mats[0], empty, empty, mats[1], empty, mats[2]]
+    xs = [X, X, X, ys[0], ys[0], ys[1]]
+    outs = [ys[0], ye[0], ye[1], ys[1], ye[2], ys[2]]
+    qg.ChainGemv(4, descs, xs, outs, [2, 1, 2, 1], flags=flags).run()
+    refs = oracle.gemv_chain(ws_np, [-1, 0, 1], [x0])
+    for y, r in zip(ys, refs):
+        assert_close(y.cpu().numpy().astype(np.float64), r)
+    assert qg.device_error() == 0
+
+
+@pytest.mark.parametrize("flags", MODES)
+def test_chain_in_cuda_graph(flags):
+    """The chain captured in a CUDA graph and replayed gives the eager call's bits."""
+    spec = [(2048, 2048, -1), (2048, 2048, 0), (16384, 2048, 1), (2048, 16384, 2)]
+    ext = [datagen.normal_f32(92, 1, 2048)]
+    ws_np, ys, ch = _run_spec(4, spec, [1, 1, 1, 1], ext, flags, 950)
+    eager = [y.clone() for y in ys]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ch.run()
+    for _ in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager, ys):
+            assert torch.equal(a, b)
+    refs = oracle.gemv_chain(ws_np, [s_ for _, _, s_ in spec], ext, _oracle_fn)
+    for y, r in zip(ys, refs):
+        assert_close(y.cpu().numpy().astype(np.float64), r)

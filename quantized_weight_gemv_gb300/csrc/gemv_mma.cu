@@ -21,10 +21,12 @@
 //    from the quantisation: each float4 of x quantises to exactly one 8-byte fragment.
 //  * the activation image is made once per call into a workspace (prep kernel) and
 //    pulled into shared memory with one bulk copy; 16 warps per CTA share it.
-//  * each warp owns tiles of 16 rows x 8 blocks and streams them through a private
-//    two-stage cp.async ring (rows padded to 144 bytes so that the fragment reads
-//    are bank-conflict free); the warps of a row group split k and their partial
-//    sums meet in shared memory.
+//  * a warp's task is one half of the k range of one group of 16 rows: 1-4 tiles of
+//    16 rows x 8 blocks, all put in flight at once through a private cp.async ring
+//    (rows padded to 144 bytes so that the fragment reads are bank-conflict free);
+//    warps w and w^1 take the two halves of a row group and add their partial sums
+//    through shared memory under a named barrier of the pair (half 0 + half 1, in
+//    that order).
 #include <cuda_fp16.h>
 
 #include "qg_internal.h"
@@ -34,7 +36,10 @@ namespace mma {
 
 constexpr int KC = 8;     // blocks per tile (256 elements of k)
 constexpr int NW = 16;    // warps per CTA
-constexpr int DEPTH = 2;  // tiles in flight per warp
+// tiles in flight per warp: as many as shared memory holds at k = 2048 (a warp's task is
+// one to four tiles, issued at once so that their DRAM latency is paid about once)
+template <int NT>
+__host__ __device__ constexpr int depth_of() { return NT == 1 ? 4 : 3; }
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -89,7 +94,7 @@ constexpr int TILE_BYTES = TILE_CODES + 2 * 16 * 16;
 
 // Shared layout: frag[nb][2][NT][32] uint2 | sv[nb][8*NT] f32 | Sv[nb][8*NT] f32 (the
 // activation image, also the workspace layout) | part[NW][16][8*NT] f32 |
-// tiles[NW][DEPTH]
+// tiles[NW][depth_of<NT>()]
 template <int NT>
 struct Smem {
     __host__ __device__ static size_t frag_bytes(int nb) { return (size_t)nb * 2 * NT * 32 * 8; }
@@ -97,7 +102,7 @@ struct Smem {
     __host__ __device__ static size_t Sv_off(int nb) { return sv_off(nb) + (size_t)nb * 8 * NT * 4; }
     __host__ __device__ static size_t part_off(int nb) { return Sv_off(nb) + (size_t)nb * 8 * NT * 4; }
     __host__ __device__ static size_t tiles_off(int nb) { return part_off(nb) + (size_t)NW * 16 * 8 * NT * 4; }
-    __host__ __device__ static size_t bytes(int nb) { return tiles_off(nb) + (size_t)NW * DEPTH * TILE_BYTES; }
+    __host__ __device__ static size_t bytes(int nb) { return tiles_off(nb) + (size_t)NW * depth_of<NT>() * TILE_BYTES; }
 };
 
 // Quantise the B activation columns straight into B fragments (image layout as
@@ -178,6 +183,9 @@ __global__ void __launch_bounds__(256) mma_prep_kernel(const float* __restrict__
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// named barrier of the two warps holding one row group's k halves
+__device__ __forceinline__ void pair_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -213,19 +221,27 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ __align__(8) uint64_t img_bar;
     const int nb = p.k >> 5;
-    const int QC = nb / KC;  // warps per row group (k split): 2, 4 or 8
-    const int RG = NW / QC;  // row groups per CTA pass
+    constexpr int DEPTH = depth_of<NT>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int my_rg = warp / QC, my_q = warp % QC;
     const int n_groups = (p.n + 15) >> 4;
     unsigned char* tiles = sm + Smem<NT>::tiles_off(nb) + (size_t)warp * DEPTH * TILE_BYTES;
 
+    // tasks: (row group, k half); warp w and w^1 hold the two halves of one row group
+    const int half_nb = nb >> 1;
+    const int TPT = half_nb / KC;  // tiles per task: 1, 2 or 4
+    const int n_tasks = 2 * n_groups;
+    const int wstride = gridDim.x * NW;
+    const int task0 = blockIdx.x * NW + warp;
+    const int my_tasks = task0 < n_tasks ? (n_tasks - task0 + wstride - 1) / wstride : 0;
+    const int n_tiles = my_tasks * TPT;
+    auto tile_rg = [&](int q) { return (task0 + (q / TPT) * wstride) >> 1; };
+    auto tile_blk = [&](int q) { return (warp & 1) * half_nb + (q % TPT) * KC; };
+
     // weights do not depend on earlier work: start the first tiles before waiting for it
-    auto group_of = [&](int pass) { return (blockIdx.x + pass * gridDim.x) * RG + my_rg; };
 #pragma unroll
     for (int d = 0; d < DEPTH; ++d) {
-        if (group_of(d) < n_groups) issue_tile(p, tiles + d * TILE_BYTES, group_of(d) * 16, my_q * KC, lane);
+        if (d < n_tiles) issue_tile(p, tiles + d * TILE_BYTES, tile_rg(d) * 16, tile_blk(d), lane);
         cp_async_commit();
     }
 
@@ -273,21 +289,25 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
     const float* Sv = reinterpret_cast<const float*>(sm + Smem<NT>::Sv_off(nb));
     float* part = reinterpret_cast<float*>(sm + Smem<NT>::part_off(nb));
 
-    for (int pass = 0; (blockIdx.x + pass * gridDim.x) * RG < n_groups; ++pass) {
-        const int base = (blockIdx.x + pass * gridDim.x) * RG;
-        const int grp = base + my_rg;
-        const unsigned char* tile = tiles + (pass % DEPTH) * TILE_BYTES;
-        cp_async_wait<DEPTH - 1>();
-        __syncwarp();
+    float* mine = part + (size_t)warp * 16 * 8 * NT;
+    const float* other = part + (size_t)(warp ^ 1) * 16 * 8 * NT;
+    const int pair_bar = 1 + (warp >> 1);
+    for (int task = 0; task < my_tasks; ++task) {
+        const int rg = (task0 + task * wstride) >> 1;
         float acc[NT][4];
 #pragma unroll
         for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-        if (grp < n_groups) {
+        for (int jt = 0; jt < TPT; ++jt) {
+            const int q = task * TPT + jt;
+            const unsigned char* tile = tiles + (q % DEPTH) * TILE_BYTES;
+            cp_async_wait<DEPTH - 1>();
+            __syncwarp();
             const unsigned short* dsc = reinterpret_cast<const unsigned short*>(tile + TILE_CODES);
             const unsigned short* dmn = dsc + 128;
+            const int blk0 = tile_blk(q);
 #pragma unroll
             for (int j = 0; j < KC; ++j) {
-                const int b = my_q * KC + j;
+                const int b = blk0 + j;
                 const uint32_t w0 = *reinterpret_cast<const uint32_t*>(tile + g * TILE_ROW + j * 16 + 4 * t);
                 const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + (g + 8) * TILE_ROW + j * 16 + 4 * t);
                 uint32_t alo[4], ahi[4];
@@ -310,15 +330,13 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
                     acc[tt][3] = fmaf(s2.y, fmaf(d1, D[3], m1 * S2.y), acc[tt][3]);
                 }
             }
+            __syncwarp();
+            // refill this slot with tile q + DEPTH (an empty group keeps the count)
+            if (q + DEPTH < n_tiles)
+                issue_tile(p, tiles + (q % DEPTH) * TILE_BYTES, tile_rg(q + DEPTH) * 16, tile_blk(q + DEPTH), lane);
+            cp_async_commit();
         }
-        __syncwarp();
-        // refill this slot with the tile of pass + DEPTH (an empty group keeps the count)
-        if (group_of(pass + DEPTH) < n_groups)
-            issue_tile(p, tiles + (pass % DEPTH) * TILE_BYTES, group_of(pass + DEPTH) * 16, my_q * KC, lane);
-        cp_async_commit();
-
-        // partial sums of the QC k-split warps of each row group meet in shared memory
-        float* mine = part + (size_t)warp * 16 * 8 * NT;
+        // the two k halves of the row group meet: half 1 leaves its sums, half 0 adds them
 #pragma unroll
         for (int tt = 0; tt < NT; ++tt) {
             mine[g * 8 * NT + tt * 8 + 2 * t] = acc[tt][0];
@@ -326,19 +344,15 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
             mine[(g + 8) * 8 * NT + tt * 8 + 2 * t] = acc[tt][2];
             mine[(g + 8) * 8 * NT + tt * 8 + 2 * t + 1] = acc[tt][3];
         }
-        __syncthreads();
-        for (int o = threadIdx.x; o < RG * 16 * 8 * NT; o += NW * 32) {
-            const int rg = o / (16 * 8 * NT);
-            const int rem = o - rg * 16 * 8 * NT;
-            const int r = rem / (8 * NT), c = rem - r * 8 * NT;
-            const int row = (base + rg) * 16 + r;
-            if (c < p.batch && row < p.n) {
-                float s = 0.0f;
-                for (int q = 0; q < QC; ++q) s += part[((size_t)(rg * QC + q) * 16 + r) * 8 * NT + c];
-                p.y[(size_t)c * p.n + row] = s;
+        pair_sync(pair_bar);
+        if ((warp & 1) == 0) {
+            for (int o = lane; o < 16 * 8 * NT; o += 32) {
+                const int r = o / (8 * NT), c = o - r * 8 * NT;
+                const int row = rg * 16 + r;
+                if (c < p.batch && row < p.n) p.y[(size_t)c * p.n + row] = mine[o] + other[o];
             }
         }
-        __syncthreads();
+        pair_sync(pair_bar);  // both partial arrays are free for the next task
     }
     cp_async_wait<0>();
 }
@@ -358,11 +372,10 @@ size_t mma_workspace_bytes(int k, int batch) {
 template <int NT>
 static int launch_mma_t(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc) {
     const int nb = p.k >> 5;
-    const int QC = nb / mma::KC, RG = mma::NW / QC;
     const int n_groups = (p.n + 15) >> 4;
     const size_t smem = mma::Smem<NT>::bytes(nb);
     if (smem > (size_t)lc.max_smem_optin - 1024) return QG_ERR_UNSUPPORTED;
-    int grid = (n_groups + RG - 1) / RG;
+    int grid = (2 * n_groups + mma::NW - 1) / mma::NW;  // one (row group, k half) task per warp
     if (grid > lc.sm_count) grid = lc.sm_count;
     if (grid < 1) grid = 1;
     if (!ws) {

@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
     cc = ic;
 
     const uint64_t pol = stream::policy_evict_first();
-    auto issue = [&](int t) {  // stage at cursor ic into slot t % D
+    auto issue = [&](int slot) {  // stage at cursor ic into the given slot
         const GDesc& d = p.d[ic.d];
         const int nb = 1 << d.log2nb;
         const int R = nb >= SBW ? 1 : SBW / nb;
@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
         const int rows_u = R == 1 ? 1 : min(R, d.n - ul * R);
         const uint32_t blocks = (uint32_t)(nb >= SBW ? SBW : rows_u * nb);
         const size_t blk0 = (size_t)ul * R * nb + (size_t)ic.part * SBW;
-        unsigned char* st = slots + (size_t)(t % D) * SL::BYTES;
-        uint64_t* bar = &full[t % D];
+        unsigned char* st = slots + (size_t)slot * SL::BYTES;
+        uint64_t* bar = &full[slot];
         stream::mbar_arrive_expect_tx(bar, blocks * SL::BPB);
         stream::bulk_g2s(st, d.lo + blk0 * 16, blocks * 16, bar, pol);
         if constexpr (BITS == 6) stream::bulk_g2s(st + SL::HI, d.hi + blk0 * 8, blocks * 8, bar, pol);
@@ -255,9 +255,11 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
     int xd = -1;  // descriptor whose activation words are in registers
     float rowacc = 0.0f;
 
-    for (int t = 0; cc.g < u_end; ++t) {
-        const int slot = t % D;
-        if (!__all_sync(0xffffffffu, stream::mbar_wait(&full[slot], (uint32_t)((t / D) & 1)))) {  // warp-uniform
+    // slot = t % D and its phase parity (t / D) & 1 of stage t, as running counters
+    int slot = 0;
+    uint32_t phase = 0;
+    for (; cc.g < u_end; slot = slot + 1 == D ? 0 : slot + 1, phase ^= slot == 0) {
+        if (!__all_sync(0xffffffffu, stream::mbar_wait(&full[slot], phase))) {  // warp-uniform
             atomicOr(p.err, ERR_WAIT_FULL);
             break;
         }
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
         __syncwarp();
         if (lane == 0 && ic.g < u_end) {
             stream::fence_proxy_async();
-            issue(t + D);
+            issue(slot);
             ic.advance(p);
         }
 

@@ -83,17 +83,26 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Slot layout: codes[256][CODE] | [hi[256][8]] | scale[256] | [min[256]]
+// Slot layout for SB blocks: codes[SB][CODE] | [hi[SB][8]] | scale[SB] | [min[SB]]
 // (Q4/Q6: 16-byte code blocks; Q2: 8-byte code blocks and no min plane)
-template <int BITS>
+template <int BITS, int SB = SBW>
 struct Slot {
     static constexpr int CODE = BITS == 2 ? 8 : 16;
     static constexpr int BPB = CODE + (BITS == 6 ? 8 : 0) + (BITS == 2 ? 2 : 4);
-    static constexpr int BYTES = SBW * BPB;
-    static constexpr int HI = SBW * 16;
-    static constexpr int SC = SBW * (CODE + (BITS == 6 ? 8 : 0));
-    static constexpr int MN = SC + SBW * 2;
+    static constexpr int BYTES = SB * BPB;
+    static constexpr int HI = SB * 16;
+    static constexpr int SC = SB * (CODE + (BITS == 6 ? 8 : 0));
+    static constexpr int MN = SC + SB * 2;
 };
+
+// Blocks per stage of the single-matrix kernel.  A Q2 block is 10 bytes against 20 for
+// Q4, so for one column and rows of at least 32 blocks a Q2 stage holds 512 blocks
+// (the same 5 KB), which halves the per-stage work (ring wait, copy issue, the row
+// reduction and the epilogue) per block.
+template <int BITS, int BC, int NB>
+__host__ __device__ constexpr int stage_blocks() {
+    return BITS == 2 && BC == 1 && NB >= 32 ? 2 * SBW : SBW;
+}
 
 // Halving reduction over the lane bits [0, LOG2SEG): V values per lane, each to be
 // summed over the 2^LOG2SEG lanes of a segment.  Step s pairs lanes across bit
@@ -127,11 +136,11 @@ __device__ __forceinline__ void halving_reduce(float (&v)[V]) {
     for (; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
 }
 
-// Row (within a 240-block stage of 48-block rows) of lane l's block l + 32j: lanes
-// 0-15 meet rows 0,0,1,2,2,3,4,4 and lanes 16-31 rows 0,1,1,2,3,3,4,5 (5: past the
-// stage).
+// Row (within a stage of whole 48-block rows) of lane l's block l + 32j.  Every three
+// j cover 96 blocks, two rows: lanes 0-15 meet rows 0,0,1 and lanes 16-31 rows 0,1,1 of
+// the pair, so the row is 2 (j / 3) plus that offset (j is a compile-time constant).
 __device__ __forceinline__ int row48(int j, int lane) {
-    return lane < 16 ? (0x44322100 >> (4 * j)) & 15 : (0x54332110 >> (4 * j)) & 15;
+    return 2 * (j / 3) + (j % 3 == 2 ? 1 : j % 3 == 1 ? (lane >= 16) : 0);
 }
 
 // byte offset of the activation columns after `nslots` slots and their mbarriers
@@ -159,18 +168,22 @@ __device__ __forceinline__ void emit_row(const StreamParams& p, long long row, c
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v >> 1); }
 
 // NB = k / 32 blocks per row: a power of two from 8 to 512, or 48 (k = 1536).  For 48 a
-// stage holds 5 whole rows (240 blocks), the activation words come from shared memory
-// and each row is summed over the warp on its own (GEN below).
+// stage holds whole rows (5 in 240 blocks, or 10 in 480 for the 512-block Q2 stage) and
+// the rows, which straddle the lanes' block groups, are summed per lane and then
+// through one halving tree (GEN below).
 template <int BITS, int BC, int EPI, int NB>
 __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(StreamParams p) {
-    using SL = Slot<BITS>;
+    constexpr int SB = stage_blocks<BITS, BC, NB>();  // blocks per stage (capacity)
+    constexpr int JL = SB / 32;                        // blocks per lane per stage
+    using SL = Slot<BITS, SB>;
     constexpr bool GEN = (NB & (NB - 1)) != 0;       // not a power of two
     constexpr int LOG2NB = GEN ? 0 : ilog2(NB);
-    constexpr int R = NB >= SBW ? 1 : SBW / NB;       // rows per stage
-    constexpr int PARTS = NB > SBW ? NB / SBW : 1;    // stages per row
+    constexpr int R = NB >= SB ? 1 : SB / NB;         // rows per stage
+    constexpr int PARTS = NB > SB ? NB / SB : 1;      // stages per row
+    constexpr int JU = GEN ? (R * NB + 31) / 32 : JL;  // blocks per lane that can be in a stage
     // distinct activation blocks per lane.  GEN (48 blocks per row): lane l meets blocks
     // (l + 32j) mod 48, and 96 = 0 mod 48, so only the three of j mod 3
-    constexpr int NXB = GEN ? 3 : NB >= 32 ? (NB < SBW ? NB / 32 : 8) : 1;
+    constexpr int NXB = GEN ? 3 : NB >= 32 ? (NB < SB ? NB / 32 : JL) : 1;
     constexpr bool XREG = NB <= 128 && BC * NXB <= 8;  // activation words in registers
     constexpr int NXR = XREG ? NXB : 1;
     static_assert(!GEN || NB == 48, "blocks per row: a power of two, or 48");
@@ -189,21 +202,21 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     const long long r0 = (long long)blockIdx.x * p.n / gridDim.x;
     const long long r1 = (long long)(blockIdx.x + 1) * p.n / gridDim.x;
     const int nrows = (int)(r1 - r0);
-    const int nunits = NB >= SBW ? nrows : (nrows + R - 1) / R;      // unit: R rows, or one row
+    const int nunits = NB >= SB ? nrows : (nrows + R - 1) / R;       // unit: R rows, or one row
     const int my_units = nunits > warp ? (nunits - warp + W - 1) / W : 0;
     const int my_stages = my_units * PARTS;
 
     const uint64_t pol = policy_evict_first();
     // issue stage t of this warp (unit warp + W*(t/PARTS), part t%PARTS) into slot t%D
-    auto issue = [&](int t) {
+    auto issue = [&](int t, int slot) {
         const int u = warp + W * (t / PARTS);
         const int part = t % PARTS;
         const long long row = r0 + (long long)u * R;
         const int rows_u = R == 1 ? 1 : min(R, nrows - u * R);
-        const uint32_t blocks = (uint32_t)(NB >= SBW ? SBW : rows_u * NB);
-        const size_t blk0 = (size_t)row * NB + (size_t)part * SBW;  // first block in the matrix
-        unsigned char* st = slots + (size_t)(t % D) * SL::BYTES;
-        uint64_t* bar = &full[t % D];
+        const uint32_t blocks = (uint32_t)(NB >= SB ? SB : rows_u * NB);
+        const size_t blk0 = (size_t)row * NB + (size_t)part * SB;  // first block in the matrix
+        unsigned char* st = slots + (size_t)slot * SL::BYTES;
+        uint64_t* bar = &full[slot];
         mbar_arrive_expect_tx(bar, blocks * SL::BPB);
         bulk_g2s(st, p.lo + blk0 * SL::CODE, blocks * SL::CODE, bar, pol);
         if constexpr (BITS == 6) bulk_g2s(st + SL::HI, p.hi + blk0 * 8, blocks * 8, bar, pol);
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         pdl_launch_dependents();
         for (int s = 0; s < D; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
-        for (int t = 0; t < D && t < my_stages; ++t) issue(t);
+        for (int t = 0; t < D && t < my_stages; ++t) issue(t, t);
     }
     __syncwarp();
 
@@ -248,9 +261,11 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
 #pragma unroll
     for (int c = 0; c < BC; ++c) rowacc[c] = 0.0f;
 
-    for (int t = 0; t < my_stages; ++t) {
-        const int slot = t % D;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (uint32_t)((t / D) & 1)))) {  // warp-uniform
+    // slot = t % D and its phase parity (t / D) & 1, kept as running counters
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int t = 0; t < my_stages; ++t, slot = slot + 1 == D ? 0 : slot + 1, phase ^= slot == 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], phase))) {  // warp-uniform
             atomicOr(p.err, ERR_WAIT_FULL);
             break;
         }
@@ -261,11 +276,11 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         const unsigned char* st = slots + (size_t)slot * SL::BYTES;
 
         // stage -> registers
-        uint4 cw[JPL];
-        uint2 hw[JPL];
-        unsigned short dh[JPL], mh[JPL];
+        uint4 cw[JU];
+        uint2 hw[JU];
+        unsigned short dh[JU], mh[JU];
 #pragma unroll
-        for (int j = 0; j < JPL; ++j) {
+        for (int j = 0; j < JU; ++j) {
             const int fb = lane + 32 * j;
             if constexpr (BITS == 2) {
                 cw[j] = make_uint4(0u, 0u, 0u, 0u);
@@ -284,14 +299,14 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         __syncwarp();
         if (lane == 0 && t + D < my_stages) {
             fence_proxy_async();  // the slot's generic reads are done before the async refill
-            issue(t + D);
+            issue(t + D, slot);
         }
 
         // block partials: part j of the lane belongs to row (lane + 32j) / NB of the stage
-        float pj[BC][JPL];
+        float pj[BC][JU];
 #pragma unroll
-        for (int j = 0; j < JPL; ++j) {
-            const int rloc = (NB >= SBW) ? 0 : GEN ? row48(j, lane) : ((lane + 32 * j) >> LOG2NB);
+        for (int j = 0; j < JU; ++j) {
+            const int rloc = (NB >= SB) ? 0 : GEN ? row48(j, lane) : ((lane + 32 * j) >> LOG2NB);
 
             const float d = half_bits_to_float(dh[j]);
             const float m = BITS == 2 ? -2.0f * d : half_bits_to_float(mh[j]);  // Q2: zero point 2
@@ -303,7 +318,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
                     const int xj = NB >= 32 ? (j % NXR) : 0;
                     r = block_combine(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), d, m, xs[c][xj], xS[c][xj]);
                 } else {
-                    const int blk = GEN ? (lane + 32 * j) % NB : (part * SBW + lane + 32 * j) & (NB - 1);
+                    const int blk = GEN ? (lane + 32 * j) % NB : (part * SB + lane + 32 * j) & (NB - 1);
                     const XqView v = xq_view(xqbase + c * xstride, NB);
                     const uint4 a = *reinterpret_cast<const uint4*>(v.lo + 16 * blk);
                     const uint4 b = *reinterpret_cast<const uint4*>(v.hi + 16 * blk);
@@ -315,23 +330,28 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
 
         if constexpr (GEN) {
             // rows straddle the lanes' block groups (row48): each lane sums its blocks per
-            // row, the 5 rows padded to 8 go through one halving tree (lane l ends with row
-            // l / 4); pj of a block outside the stage's rows is already 0
+            // row, rows 2i and 2i+1 from j = 3i, 3i+1 (lanes 0-15: row 2i; 16-31: 2i+1) and
+            // 3i+2; the R rows padded to RV go through one halving tree, after which lane l
+            // holds row l / (32 / RV).  pj of a block outside the stage's rows is already 0
+            constexpr int RV = R <= 8 ? 8 : 16;
             const bool lo = lane < 16;
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
-                float rs[8];
-                rs[0] = pj[c][0] + (lo ? pj[c][1] : 0.0f);
-                rs[1] = (lo ? 0.0f : pj[c][1]) + pj[c][2];
-                rs[2] = pj[c][3] + (lo ? pj[c][4] : 0.0f);
-                rs[3] = (lo ? 0.0f : pj[c][4]) + pj[c][5];
-                rs[4] = pj[c][6] + (lo ? pj[c][7] : 0.0f);
-                rs[5] = rs[6] = rs[7] = 0.0f;
-                halving_reduce<8, 5>(rs);
+                float rs[RV];
+#pragma unroll
+                for (int i = 0; i < RV / 2; ++i) {
+                    const float a = 3 * i < JU ? pj[c][3 * i < JU ? 3 * i : 0] : 0.0f;
+                    const float b = 3 * i + 1 < JU ? pj[c][3 * i + 1 < JU ? 3 * i + 1 : 0] : 0.0f;
+                    const float e = 3 * i + 2 < JU ? pj[c][3 * i + 2 < JU ? 3 * i + 2 : 0] : 0.0f;
+                    rs[2 * i] = a + (lo ? b : 0.0f);
+                    rs[2 * i + 1] = (lo ? 0.0f : b) + e;
+                }
+                halving_reduce<RV, 5>(rs);
                 pj[c][0] = rs[0];
             }
-            if ((lane & 3) == 0) {
-                const int r = lane >> 2;
+            constexpr int LPR = 32 / RV;  // lanes holding one row's total
+            if ((lane & (LPR - 1)) == 0) {
+                const int r = lane / LPR;
                 if (r < rows_u) {
                     float out[BC];
 #pragma unroll
@@ -340,8 +360,8 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
                 }
             }
         } else if constexpr (NB >= 32) {
-            // R rows per stage, JPL/R consecutive j per row
-            constexpr int JR = JPL / R;
+            // R rows per stage, JL/R consecutive j per row
+            constexpr int JR = JL / R;
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
                 float rs[R];
@@ -380,8 +400,8 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         } else {
             // NB < 32: value j of lane l is row j*(32/NB) + l/NB, summed over NB-lane segments
 #pragma unroll
-            for (int c = 0; c < BC; ++c) halving_reduce<JPL, LOG2NB>(pj[c]);
-            constexpr int KEEP = NB / JPL;  // lanes holding the same value after the halving steps
+            for (int c = 0; c < BC; ++c) halving_reduce<JL, LOG2NB>(pj[c]);
+            constexpr int KEEP = NB / JL;  // lanes holding the same value after the halving steps
             if ((lane & (KEEP - 1)) == 0) {
                 const int v = (lane & (NB - 1)) / KEEP;
                 const int r = v * (32 / NB) + lane / NB;

@@ -16,7 +16,7 @@ inline int env_int(const char* name, int dflt) {
 
 template <int BITS, int BC, int EPI, int NB>
 int launch_t(StreamParams p, const LaunchCtx& lc) {
-    using SL = Slot<BITS>;
+    using SL = Slot<BITS, stage_blocks<BITS, BC, NB>()>;
     auto kern = gemv_stream_kernel<BITS, BC, EPI, NB>;
     constexpr int W = 8;  // warps per CTA
     const size_t fixed = (size_t)BC * xq_stride(NB);

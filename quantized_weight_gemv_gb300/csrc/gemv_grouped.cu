@@ -443,7 +443,10 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
          {grouped_gemv_kernel<6, 2, false>, grouped_gemv_kernel<6, 2, true>}}};
     const K kern = kerns[bits == 4 ? 0 : 1][per_sm - 1][smx ? 1 : 0];
     if (int e = ensure_smem_attr((const void*)kern, smem, lc)) return e;
-    long long grid = (long long)lc.sm_count * per_sm;
+    int grid_per_sm = env_int("QG_GROUPED_GRID_PER_SM", per_sm);
+    if (grid_per_sm < 1) grid_per_sm = 1;
+    if (grid_per_sm > 2) grid_per_sm = 2;
+    long long grid = (long long)lc.sm_count * grid_per_sm;
     if (grid > units) grid = units;
     LaunchCtx lc2 = lc;
     if (!smx) lc2.flags |= QG_FLAG_PDL;

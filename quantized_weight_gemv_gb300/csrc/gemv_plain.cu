@@ -46,15 +46,15 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
                 cw = ldg_stream16(crow + 16 * (size_t)b);
                 if constexpr (BITS == 6) hw = ldg_stream8(hrow + 8 * (size_t)b);
             }
-            const float d = half_bits_to_float(ldg_stream2(srow + b));
-            const float m = BITS == 2 ? -2.0f * d : half_bits_to_float(ldg_stream2(mrow + b));
+            const unsigned short dh = ldg_stream2(srow + b);
+            const unsigned short mh = BITS == 2 ? (unsigned short)0 : ldg_stream2(mrow + b);
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
                 if (c < p.batch) {
                     const XqView v = xq_view(smem + c * xstride, nb);
                     const uint4 xl = *reinterpret_cast<const uint4*>(v.lo + 16 * b);
                     const uint4 xh = *reinterpret_cast<const uint4*>(v.hi + 16 * b);
-                    acc[c] += block_combine(qdot<BITS>(cw, hw, xl, xh), d, m, v.s[b], v.S[b]);
+                    acc[c] += combine<BITS>(qdot<BITS>(cw, hw, xl, xh), dh, mh, v.s[b], v.S[b]);
                 }
             }
         }

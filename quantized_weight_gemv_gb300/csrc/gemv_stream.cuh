@@ -136,13 +136,6 @@ __device__ __forceinline__ void halving_reduce(float (&v)[V]) {
     for (; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
 }
 
-// Row (within a stage of whole 48-block rows) of lane l's block l + 32j.  Every three
-// j cover 96 blocks, two rows: lanes 0-15 meet rows 0,0,1 and lanes 16-31 rows 0,1,1 of
-// the pair, so the row is 2 (j / 3) plus that offset (j is a compile-time constant).
-__device__ __forceinline__ int row48(int j, int lane) {
-    return 2 * (j / 3) + (j % 3 == 2 ? 1 : j % 3 == 1 ? (lane >= 16) : 0);
-}
-
 // byte offset of the activation columns after `nslots` slots and their mbarriers
 __host__ __device__ constexpr size_t xq_offset(int nslots, int slot_bytes) {
     return (((size_t)nslots * (size_t)(slot_bytes + 8)) + 15) & ~(size_t)15;
@@ -302,37 +295,35 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
             issue(t + D, slot);
         }
 
-        // block partials: part j of the lane belongs to row (lane + 32j) / NB of the stage
+        // block partials: part j of the lane belongs to row (lane + 32j) / NB of the stage.
+        // In a stage of fewer than R rows the blocks past its last row are computed on
+        // stale slot bytes; every reduction below keeps rows apart and only the stage's
+        // rows are emitted, so they are never masked here.
         float pj[BC][JU];
 #pragma unroll
         for (int j = 0; j < JU; ++j) {
-            const int rloc = (NB >= SB) ? 0 : GEN ? row48(j, lane) : ((lane + 32 * j) >> LOG2NB);
-
-            const float d = half_bits_to_float(dh[j]);
-            const float m = BITS == 2 ? -2.0f * d : half_bits_to_float(mh[j]);  // Q2: zero point 2
-            const bool valid = rloc < rows_u;
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
-                float r;
                 if constexpr (XREG) {
                     const int xj = NB >= 32 ? (j % NXR) : 0;
-                    r = block_combine(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), d, m, xs[c][xj], xS[c][xj]);
+                    pj[c][j] = combine<BITS>(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), dh[j], mh[j], xs[c][xj],
+                                             xS[c][xj]);
                 } else {
                     const int blk = GEN ? (lane + 32 * j) % NB : (part * SB + lane + 32 * j) & (NB - 1);
                     const XqView v = xq_view(xqbase + c * xstride, NB);
                     const uint4 a = *reinterpret_cast<const uint4*>(v.lo + 16 * blk);
                     const uint4 b = *reinterpret_cast<const uint4*>(v.hi + 16 * blk);
-                    r = block_combine(qdot<BITS>(cw[j], hw[j], a, b), d, m, v.s[blk], v.S[blk]);
+                    pj[c][j] = combine<BITS>(qdot<BITS>(cw[j], hw[j], a, b), dh[j], mh[j], v.s[blk], v.S[blk]);
                 }
-                pj[c][j] = valid ? r : 0.0f;
             }
         }
 
         if constexpr (GEN) {
-            // rows straddle the lanes' block groups (row48): each lane sums its blocks per
-            // row, rows 2i and 2i+1 from j = 3i, 3i+1 (lanes 0-15: row 2i; 16-31: 2i+1) and
-            // 3i+2; the R rows padded to RV go through one halving tree, after which lane l
-            // holds row l / (32 / RV).  pj of a block outside the stage's rows is already 0
+            // rows straddle the lanes' block groups: block l + 32j of lane l lies in row
+            // (l + 32j) / 48, and every three j cover 96 blocks, two rows - j = 3i is in
+            // row 2i, j = 3i+1 in row 2i (lanes 0-15) or 2i+1 (lanes 16-31), j = 3i+2 in
+            // row 2i+1.  Each lane sums its blocks per row; the R rows padded to RV go
+            // through one halving tree, after which lane l holds row l / (32 / RV)
             constexpr int RV = R <= 8 ? 8 : 16;
             const bool lo = lane < 16;
 #pragma unroll

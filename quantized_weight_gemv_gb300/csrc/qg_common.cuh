@@ -202,19 +202,21 @@ __device__ __forceinline__ int block_dot_q4(uint4 c, uint4 xlo, uint4 xhi) {
 // Q2 block dot from its 8 code bytes (word h0 = bytes 0..3, h1 = bytes 4..7; byte t
 // holds codes t, t+8, t+16, t+24 at bit pairs 0..3).  Bit pair s of h0 / h1 meets the
 // activation word 2s / 2s+1 of the block (elements 8s..8s+3 / 8s+4..8s+7), i.e. words
-// of the low half for s < 2 and of the high half for s >= 2.  The pairs are masked in
-// place (4^s * code, at most 192) and dotted as unsigned bytes; the four sums are
-// exact multiples of 4^s.
+// of the low half for s < 2 and of the high half for s >= 2.  Pairs 0 and 2 are masked
+// in place in the code word, pairs 1 and 3 in the word shifted right by 2, so pairs
+// 0/1 count once and pairs 2/3 sixteen times (codes of at most 48 as unsigned bytes):
+// the dot is the first sum plus the second, an exact multiple of 16, divided by 16.
 __device__ __forceinline__ int block_dot_q2(uint2 c, uint4 xlo, uint4 xhi) {
-    int a0 = __dp4a((int)(c.x & 0x03030303u), (int)xlo.x, 0);
-    a0 = __dp4a((int)(c.y & 0x03030303u), (int)xlo.y, a0);
-    int a1 = dp4a_us(c.x & 0x0C0C0C0Cu, xlo.z, 0);
-    a1 = dp4a_us(c.y & 0x0C0C0C0Cu, xlo.w, a1);
-    int a2 = dp4a_us(c.x & 0x30303030u, xhi.x, 0);
-    a2 = dp4a_us(c.y & 0x30303030u, xhi.y, a2);
-    int a3 = dp4a_us(c.x & 0xC0C0C0C0u, xhi.z, 0);
-    a3 = dp4a_us(c.y & 0xC0C0C0C0u, xhi.w, a3);
-    return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
+    const uint32_t sx = c.x >> 2, sy = c.y >> 2;
+    int a = __dp4a((int)(c.x & 0x03030303u), (int)xlo.x, 0);
+    a = __dp4a((int)(c.y & 0x03030303u), (int)xlo.y, a);
+    a = __dp4a((int)(sx & 0x03030303u), (int)xlo.z, a);
+    a = __dp4a((int)(sy & 0x03030303u), (int)xlo.w, a);
+    int b = dp4a_us(c.x & 0x30303030u, xhi.x, 0);
+    b = dp4a_us(c.y & 0x30303030u, xhi.y, b);
+    b = dp4a_us(sx & 0x30303030u, xhi.z, b);
+    b = dp4a_us(sy & 0x30303030u, xhi.w, b);
+    return a + (b >> 4);
 }
 
 // block dot of any format from its raw words: Q4 cw; Q6 cw and hw; Q2 hw (8 code bytes)
@@ -237,6 +239,23 @@ __device__ __forceinline__ int qdot(uint4 cw, uint2 hw, uint4 xlo, uint4 xhi) {
 // s_b * (scale * D + min * S_b) in fp32
 __device__ __forceinline__ float block_combine(int D, float d, float m, float s, float S) {
     return s * fmaf(d, (float)D, m * S);
+}
+
+// Q2 (w = scale * (code - 2)): s_b * scale * (D - 2 S_b), the integer factor exact in
+// fp32 (|D|, |S_b| < 2^14)
+__device__ __forceinline__ float block_combine_q2(int D, float d, float s, float S) {
+    return (s * d) * fmaf(-2.0f, S, (float)D);
+}
+
+// the combine of a format from the block's binary16 scale (and min) bits
+template <int BITS>
+__device__ __forceinline__ float combine(int D, unsigned short dh, unsigned short mh, float s, float S) {
+    if constexpr (BITS == 2) {
+        (void)mh;
+        return block_combine_q2(D, half_bits_to_float(dh), s, S);
+    } else {
+        return block_combine(D, half_bits_to_float(dh), half_bits_to_float(mh), s, S);
+    }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -6,19 +6,24 @@
 // sum code * xq are computed with mma.sync m16n8k16 (f16 in, f32 accumulate), fresh
 // for every block so that the per-block scales are applied exactly as in the
 // single-column kernels:  y[c][r] += s[c] * (d[r] * D[r][c] + m[r] * S[c]).
-// Exactness: codes 0..15 (and 16 * code for the high nibbles, <= 240) and int8
-// activations are exact in f16, each product is an integer below 2^15 and each
-// 16-term dot below 2^16, so every partial sum is exact in f32.
-//
 // Operand mapping (16 weight rows x 8 columns x 16 k per mma):
 //  * the k order inside a block is permuted so that a thread's own 32-bit code word
 //    is its A fragment: thread (g = lane/4, t = lane%4) reads bytes 4t..4t+3 of the
-//    16-byte block of rows g and g+8; their low nibbles are elements 4t..4t+3 (first
-//    mma, k-slots 2t, 2t+1, 8+2t, 9+2t), their high nibbles elements 16+4t..16+4t+3
-//    (second mma).  Nibbles become f16 with the 0x6400 magic number: bits
-//    0x6400 | c read as half are 1024 + c, minus 1024 exactly.
+//    16-byte block of rows g and g+8.  Their low nibbles are elements 4t..4t+3 (first
+//    mma): bytes 0 and 2 fill k-slots 2t, 2t+1 and bytes 1 and 3 (the word shifted
+//    right by 8) k-slots 2t+8, 2t+9.  The high nibbles, elements 16+4t..16+4t+3, fill
+//    the second mma in the same order, masked in place (16 x code).  A nibble v becomes
+//    binary16 as the bits 0x6400 | v, which read as 1024 + v.
 //  * the B fragments (activations) are written in the same permuted order straight
-//    from the quantisation: each float4 of x quantises to exactly one 8-byte fragment.
+//    from the quantisation: each float4 of x quantises to exactly one 8-byte fragment;
+//    the high half holds x/16, so the second mma adds 64 x + code x per element.
+//  * the offsets come out exactly through the accumulator's initial value: the first
+//    mma starts from -(1024 X_lo + 64 X_hi), X_lo and X_hi the sums of the block's
+//    int8 activations over elements 0-15 and 16-31, so that after both mmas the
+//    accumulator holds the block dot D = sum code * xq itself.
+// Exactness: 1024 + v (v <= 240) and int8 activations (and their sixteenths) are exact
+// in f16, every product is an integer below 2^17 and every partial sum, the initial
+// value included, an integer below 2^23 in magnitude, so all of them are exact in f32.
 //  * the activation image is made once per call into a workspace (prep kernel) and
 //    pulled into shared memory with one bulk copy; 16 warps per CTA share it.
 //  * a warp's task is one half of the k range of one group of 16 rows: 1-4 tiles of
@@ -41,14 +46,6 @@ constexpr int NW = 16;    // warps per CTA
 template <int NT>
 __host__ __device__ constexpr int depth_of() { return NT == 1 ? 4 : 3; }
 
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%10,%10,%10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
-}
-
 // d = a * b + c
 __device__ __forceinline__ void mma_16816_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
                                               const float (&c)[4]) {
@@ -59,23 +56,27 @@ __device__ __forceinline__ void mma_16816_acc(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
-__device__ __forceinline__ uint32_t hsub1024(uint32_t v) {
-    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), __half2half2(__ushort_as_half(0x6400)));
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
+// two nibbles (bits 0-3 and 16-19 under `mask`, or 4-7 and 20-23) as 1024 + v in f16x2
+__device__ __forceinline__ uint32_t nib_h2(uint32_t w, uint32_t mask) { return (w & mask) | 0x64006400u; }
 
 // A fragments of one block from the code words of rows g (w0) and g+8 (w1)
 __device__ __forceinline__ void a_frags(uint32_t w0, uint32_t w1, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
-    const uint32_t p0 = __byte_perm(w0, 0u, 0x4140), q0 = __byte_perm(w0, 0u, 0x4342);
-    const uint32_t p1 = __byte_perm(w1, 0u, 0x4140), q1 = __byte_perm(w1, 0u, 0x4342);
-    lo[0] = hsub1024((p0 & 0x000F000Fu) | 0x64006400u);
-    lo[1] = hsub1024((p1 & 0x000F000Fu) | 0x64006400u);
-    lo[2] = hsub1024((q0 & 0x000F000Fu) | 0x64006400u);
-    lo[3] = hsub1024((q1 & 0x000F000Fu) | 0x64006400u);
-    hi[0] = hsub1024((p0 & 0x00F000F0u) | 0x64006400u);
-    hi[1] = hsub1024((p1 & 0x00F000F0u) | 0x64006400u);
-    hi[2] = hsub1024((q0 & 0x00F000F0u) | 0x64006400u);
-    hi[3] = hsub1024((q1 & 0x00F000F0u) | 0x64006400u);
+    const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
+    lo[0] = nib_h2(w0, 0x000F000Fu);
+    lo[1] = nib_h2(w1, 0x000F000Fu);
+    lo[2] = nib_h2(v0, 0x000F000Fu);
+    lo[3] = nib_h2(v1, 0x000F000Fu);
+    hi[0] = nib_h2(w0, 0x00F000F0u);
+    hi[1] = nib_h2(w1, 0x00F000F0u);
+    hi[2] = nib_h2(v0, 0x00F000F0u);
+    hi[3] = nib_h2(v1, 0x00F000F0u);
+}
+
+// binary16 number j (0..7) of eight packed in a uint4, as fp32
+__device__ __forceinline__ float half8_at(const uint4& v, int j) {
+    const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+    const __half2 h = *reinterpret_cast<const __half2*>(&w);
+    return (j & 1) ? __high2float(h) : __low2float(h);
 }
 
 // two int8 activations as f16, optionally divided by 16 (exact: |q|/16 has at most
@@ -92,15 +93,16 @@ constexpr int TILE_ROW = 144;
 constexpr int TILE_CODES = 16 * TILE_ROW;
 constexpr int TILE_BYTES = TILE_CODES + 2 * 16 * 16;
 
-// Shared layout: frag[nb][2][NT][32] uint2 | sv[nb][8*NT] f32 | Sv[nb][8*NT] f32 (the
-// activation image, also the workspace layout) | part[NW][16][8*NT] f32 |
-// tiles[NW][depth_of<NT>()]
+// Shared layout: frag[nb][NT][32][2] uint2 (a lane's low- and high-half B fragments
+// side by side) | sS[nb][8*NT] (s, S) f32 pairs |
+// C0[nb][8*NT] f32, the first mma's initial value (the activation image, also the
+// workspace layout) | part[NW][16][8*NT] f32 | tiles[NW][depth_of<NT>()]
 template <int NT>
 struct Smem {
     __host__ __device__ static size_t frag_bytes(int nb) { return (size_t)nb * 2 * NT * 32 * 8; }
-    __host__ __device__ static size_t sv_off(int nb) { return frag_bytes(nb); }
-    __host__ __device__ static size_t Sv_off(int nb) { return sv_off(nb) + (size_t)nb * 8 * NT * 4; }
-    __host__ __device__ static size_t part_off(int nb) { return Sv_off(nb) + (size_t)nb * 8 * NT * 4; }
+    __host__ __device__ static size_t sS_off(int nb) { return frag_bytes(nb); }
+    __host__ __device__ static size_t C0_off(int nb) { return sS_off(nb) + (size_t)nb * 8 * NT * 8; }
+    __host__ __device__ static size_t part_off(int nb) { return C0_off(nb) + (size_t)nb * 8 * NT * 4; }
     __host__ __device__ static size_t tiles_off(int nb) { return part_off(nb) + (size_t)NW * 16 * 8 * NT * 4; }
     __host__ __device__ static size_t bytes(int nb) { return tiles_off(nb) + (size_t)NW * depth_of<NT>() * TILE_BYTES; }
 };
@@ -108,8 +110,9 @@ struct Smem {
 // Quantise the B activation columns straight into B fragments (image layout as
 // Smem<NT> without the partial sums).  float4 number idx of column c (elements
 // 4m..4m+3 of block b, m = idx & 7) becomes the fragment of lane 4*(c%8) + (m%4),
-// k half m/4, tile c/8; the high half (m >= 4) holds x/16, so that its product with
-// the 16x high-nibble codes accumulates onto the low half exactly.  Items
+// tile c/8, k half m/4, as the pairs (q0, q2) and (q1, q3); the high half (m >= 4)
+// holds x/16, so that its product with the 16x high-nibble codes accumulates onto the
+// low half exactly.  Per block and column: s, S and -(1024 X_lo + 64 X_hi).  Items
 // [item0, item0 + nthreads * rounds) of the 8*NT*k/4 float4s are done by threads
 // t = 0..nthreads-1 (whole warps).
 template <int NT>
@@ -117,8 +120,8 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
                                                   int t, int nthreads, int item0, int item_end) {
     const int nb = k >> 5;
     uint2* frag = reinterpret_cast<uint2*>(img);
-    float* sv = reinterpret_cast<float*>(img + Smem<NT>::sv_off(nb));
-    float* Sv = reinterpret_cast<float*>(img + Smem<NT>::Sv_off(nb));
+    float2* sS = reinterpret_cast<float2*>(img + Smem<NT>::sS_off(nb));
+    float* C0 = reinterpret_cast<float*>(img + Smem<NT>::C0_off(nb));
     const int nf4 = k >> 2;
     const int total = min(8 * NT * nf4, item_end);  // columns beyond the batch quantise zeros
     constexpr int CHUNK = 8;
@@ -151,19 +154,19 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
                 q2 = quant_code(r.z, s, inv);
                 q3 = quant_code(r.w, s, inv);
             }
-            int S = q0 + q1 + q2 + q3;
-            S += __shfl_xor_sync(0xffffffffu, S, 1);
-            S += __shfl_xor_sync(0xffffffffu, S, 2);
-            S += __shfl_xor_sync(0xffffffffu, S, 4);
+            int H = q0 + q1 + q2 + q3;  // over the 4 float4s of this half of the block
+            H += __shfl_xor_sync(0xffffffffu, H, 1);
+            H += __shfl_xor_sync(0xffffffffu, H, 2);
+            const int Ho = __shfl_xor_sync(0xffffffffu, H, 4);  // the other half
             if (idx_all < total) {
                 const int b = idx >> 3, m = idx & 7;
                 const int lane = 4 * (c & 7) + (m & 3);
                 const bool hi = m >= 4;
-                frag[((b * 2 + (m >> 2)) * NT + (c >> 3)) * 32 + lane] =
-                    make_uint2(pack_h2(q0, q1, hi), pack_h2(q2, q3, hi));
-                if (m == 0) {
-                    sv[b * 8 * NT + c] = s;
-                    Sv[b * 8 * NT + c] = (float)S;
+                frag[((b * NT + (c >> 3)) * 32 + lane) * 2 + (m >> 2)] =
+                    make_uint2(pack_h2(q0, q2, hi), pack_h2(q1, q3, hi));
+                if (m == 0) {  // H = X_lo, Ho = X_hi
+                    sS[b * 8 * NT + c] = make_float2(s, (float)(H + Ho));
+                    C0[b * 8 * NT + c] = -(float)(1024 * H + 64 * Ho);
                 }
             }
         }
@@ -229,14 +232,15 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
 
     // tasks: (row group, k half); warp w and w^1 hold the two halves of one row group
     const int half_nb = nb >> 1;
-    const int TPT = half_nb / KC;  // tiles per task: 1, 2 or 4
+    const int TPT = half_nb / KC;                 // tiles per task: 1, 2 or 4
+    const int LT = TPT == 1 ? 0 : TPT == 2 ? 1 : 2;  // log2(TPT)
     const int n_tasks = 2 * n_groups;
     const int wstride = gridDim.x * NW;
     const int task0 = blockIdx.x * NW + warp;
     const int my_tasks = task0 < n_tasks ? (n_tasks - task0 + wstride - 1) / wstride : 0;
     const int n_tiles = my_tasks * TPT;
-    auto tile_rg = [&](int q) { return (task0 + (q / TPT) * wstride) >> 1; };
-    auto tile_blk = [&](int q) { return (warp & 1) * half_nb + (q % TPT) * KC; };
+    auto tile_rg = [&](int q) { return (task0 + (q >> LT) * wstride) >> 1; };
+    auto tile_blk = [&](int q) { return (warp & 1) * half_nb + (q & (TPT - 1)) * KC; };
 
     // weights do not depend on earlier work: start the first tiles before waiting for it
 #pragma unroll
@@ -261,17 +265,20 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
                 "l"(img), "r"(bytes), "r"(smem_u32(&img_bar))
                 : "memory");
         }
-        __syncthreads();  // the barrier is initialised before anyone polls it
-        uint32_t ok = 0;
-        const unsigned long long t0 = globaltimer_ns();
-        for (;;) {
-            asm volatile(
-                "{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n\t"
-                "selp.u32 %0, 1, 0, q;\n\t}"
-                : "=r"(ok)
-                : "r"(smem_u32(&img_bar))
-                : "memory");
-            if (ok || globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+        // thread 0 waits for the image (bounded); the block barrier below then orders the
+        // landed bytes for every other thread
+        uint32_t ok = 1;
+        if (threadIdx.x == 0) {
+            const unsigned long long t0 = globaltimer_ns();
+            for (;;) {
+                asm volatile(
+                    "{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n\t"
+                    "selp.u32 %0, 1, 0, q;\n\t}"
+                    : "=r"(ok)
+                    : "r"(smem_u32(&img_bar))
+                    : "memory");
+                if (ok || globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+            }
         }
         // give up together if the copy never landed (bounded wait), leaving the error word set
         if (__syncthreads_or(ok == 0)) {
@@ -285,8 +292,8 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
     __syncthreads();
 
     const uint2* frag = reinterpret_cast<const uint2*>(sm);
-    const float* sv = reinterpret_cast<const float*>(sm + Smem<NT>::sv_off(nb));
-    const float* Sv = reinterpret_cast<const float*>(sm + Smem<NT>::Sv_off(nb));
+    const float2* sS = reinterpret_cast<const float2*>(sm + Smem<NT>::sS_off(nb));
+    const float* C0 = reinterpret_cast<const float*>(sm + Smem<NT>::C0_off(nb));
     float* part = reinterpret_cast<float*>(sm + Smem<NT>::part_off(nb));
 
     float* mine = part + (size_t)warp * 16 * 8 * NT;
@@ -302,8 +309,11 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
             const unsigned char* tile = tiles + (q % DEPTH) * TILE_BYTES;
             cp_async_wait<DEPTH - 1>();
             __syncwarp();
-            const unsigned short* dsc = reinterpret_cast<const unsigned short*>(tile + TILE_CODES);
-            const unsigned short* dmn = dsc + 128;
+            // scale and min of rows g and g+8 for the tile's 8 blocks (16 bytes a row)
+            const uint4 dg = *reinterpret_cast<const uint4*>(tile + TILE_CODES + g * 16);
+            const uint4 dg8 = *reinterpret_cast<const uint4*>(tile + TILE_CODES + (g + 8) * 16);
+            const uint4 mg = *reinterpret_cast<const uint4*>(tile + TILE_CODES + 256 + g * 16);
+            const uint4 mg8 = *reinterpret_cast<const uint4*>(tile + TILE_CODES + 256 + (g + 8) * 16);
             const int blk0 = tile_blk(q);
 #pragma unroll
             for (int j = 0; j < KC; ++j) {
@@ -312,22 +322,23 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
                 const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + (g + 8) * TILE_ROW + j * 16 + 4 * t);
                 uint32_t alo[4], ahi[4];
                 a_frags(w0, w1, alo, ahi);
-                const float d0 = half_bits_to_float(dsc[g * 8 + j]), d1 = half_bits_to_float(dsc[(g + 8) * 8 + j]);
-                const float m0 = half_bits_to_float(dmn[g * 8 + j]), m1 = half_bits_to_float(dmn[(g + 8) * 8 + j]);
+                const float d0 = half8_at(dg, j), d1 = half8_at(dg8, j);
+                const float m0 = half8_at(mg, j), m1 = half8_at(mg8, j);
 #pragma unroll
                 for (int tt = 0; tt < NT; ++tt) {
-                    const uint2 bl = frag[((b * 2 + 0) * NT + tt) * 32 + lane];
-                    const uint2 bh = frag[((b * 2 + 1) * NT + tt) * 32 + lane];
+                    const uint4 bf = *reinterpret_cast<const uint4*>(frag + ((b * NT + tt) * 32 + lane) * 2);
+                    const int col = b * 8 * NT + tt * 8 + 2 * t;
+                    const float4 ss = *reinterpret_cast<const float4*>(sS + col);  // (s, S) of cols 2t, 2t+1
+                    const float2 c0 = *reinterpret_cast<const float2*>(C0 + col);
+                    const float cinit[4] = {c0.x, c0.y, c0.x, c0.y};
                     float dl[4], D[4];
-                    mma_16816(dl, alo, bl.x, bl.y);
-                    mma_16816_acc(D, ahi, bh.x, bh.y, dl);  // exact integer block dots
-                    const float2 s2 = *reinterpret_cast<const float2*>(sv + b * 8 * NT + tt * 8 + 2 * t);
-                    const float2 S2 = *reinterpret_cast<const float2*>(Sv + b * 8 * NT + tt * 8 + 2 * t);
+                    mma_16816_acc(dl, alo, bf.x, bf.y, cinit);
+                    mma_16816_acc(D, ahi, bf.z, bf.w, dl);  // exact integer block dots
                     // (row g, col 2t), (row g, col 2t+1), (row g+8, col 2t), (row g+8, col 2t+1)
-                    acc[tt][0] = fmaf(s2.x, fmaf(d0, D[0], m0 * S2.x), acc[tt][0]);
-                    acc[tt][1] = fmaf(s2.y, fmaf(d0, D[1], m0 * S2.y), acc[tt][1]);
-                    acc[tt][2] = fmaf(s2.x, fmaf(d1, D[2], m1 * S2.x), acc[tt][2]);
-                    acc[tt][3] = fmaf(s2.y, fmaf(d1, D[3], m1 * S2.y), acc[tt][3]);
+                    acc[tt][0] = fmaf(ss.x, fmaf(d0, D[0], m0 * ss.y), acc[tt][0]);
+                    acc[tt][1] = fmaf(ss.z, fmaf(d0, D[1], m0 * ss.w), acc[tt][1]);
+                    acc[tt][2] = fmaf(ss.x, fmaf(d1, D[2], m1 * ss.y), acc[tt][2]);
+                    acc[tt][3] = fmaf(ss.z, fmaf(d1, D[3], m1 * ss.w), acc[tt][3]);
                 }
             }
             __syncwarp();

@@ -362,6 +362,40 @@ def test_batched_tensor_core_with_and_without_workspace(batch, k):
             assert_close(Y[b], refs[b])
 
 
+@pytest.mark.parametrize("batch", [8, 12, 16])
+@pytest.mark.parametrize("k", [512, 2048])
+def test_batched_tensor_core_block_dot_exact(batch, k):
+    """The tensor-core block dot is the exact integer sum of code x int8 activation.
+
+    Only block 0 carries weight (scale 1, min 0; every other block scale 0, min 0), and
+    every column has block-0 activations that are integers of absolute maximum 127, so
+    s = 1, xq = x and each output is block 0's integer dot itself: the oracle's fp64
+    value, compared bit for bit.  Rows 0-3 and columns 0-2 reach the extremes: all codes
+    15 or 0 against all +127, all -127 and a +127 / -127 split of the block's halves."""
+    n, nb = 150, k // 32
+    rng = np.random.default_rng(7000 + k + batch)
+    q = rng.integers(0, 16, (n, k)).astype(np.uint8)
+    q[0], q[1] = 15, 0
+    q[2, :16], q[2, 16:] = 15, 0
+    q[3, :16], q[3, 16:] = 0, 15
+    scale = np.zeros((n, nb))
+    scale[:, 0] = 1.0
+    w = make_w(4, q, scale, np.zeros((n, nb)))
+    X = rng.integers(-127, 128, (batch, k)).astype(np.float32)
+    X[:, 5] = 127.0
+    X[0, :32], X[1, :32] = 127.0, -127.0
+    X[2, :16], X[2, 16:32] = 127.0, -127.0
+    wd = dev_w(w)
+    Xt = torch.from_numpy(X).to(DEV)
+    refs = [oracle.gemv(w, X[b]) for b in range(batch)]
+    for b in range(batch):  # the reference is the integer dot itself
+        assert np.array_equal(refs[b], (q[:, :32].astype(np.int64) @ X[b, :32].astype(np.int64)).astype(np.float64))
+    for ws in ("auto", None):
+        Y = qg.qgemv_batched(4, wd["lo"], None, wd["scale"], wd["min"], Xt, ws=ws).cpu().numpy()
+        for b in range(batch):
+            assert np.array_equal(Y[b].astype(np.float64), refs[b]), (ws, b)
+
+
 # ---------------------------------------------------------------- constrained selection
 def _allowed_cases(n, rng):
     yield None

@@ -32,7 +32,7 @@ METRIC = "effective weight GB/s & GEMV/s at batch 1 (fraction of ~8 TB/s HBM)"
 # full decode-layer stream (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None
 # whenever the kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "grouped": {"kernel": "grouped::grouped_gemv_kernel<4,2,0>", "bytes_per_launch": 2484.06e6},
+    "grouped": {"kernel": "grouped::grouped_gemv_kernel<4,2,0>", "bytes_per_launch": 2482.51e6},
     "percall": None,
 }
 
@@ -66,6 +66,7 @@ CASES = {
     "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
     "q4_chain_persistent": None,  # the decode chain, --layers layers (run_chain_case)
     "q4_chain_launches": None,
+    "q4_decode_stream": None,  # the --layers-layer decode stream as one grouped call (run_stream_case)
 }
 
 
@@ -93,11 +94,38 @@ def run_chain_case(args):
           flush=True)
 
 
+def run_stream_case(args):
+    """Profiling case: the decode-layer stream of --layers layers (35: 245 GEMVs, 2.48 GB) as
+    --reps eager qgemv_grouped calls - the timed path of the default run in a few launches."""
+    import torch
+
+    import quantized_weight_gemv_gb300 as qg
+    from datagen import workloads as W
+
+    device = torch.device("cuda", 0)
+    mats, xs, ys = [], [], []
+    for layer in range(args.layers):
+        for proj in range(7):
+            w, x = W.decode_projection(layer, proj)
+            mats.append(qg.to_device(w, device))
+            xs.append(torch.from_numpy(x).to(device))
+            ys.append(torch.empty(w["n"], device=device))
+    grouped = qg.GroupedGemv(4, mats, xs, ys, flags=qg.QG_FLAG_PDL)  # as the default run
+    nbytes = sum(W.q4_bytes(m["n"], m["k"]) for m in mats)
+    ms = time_eager(grouped.run, torch.cuda.current_stream(device), args.reps)
+    assert qg.device_error() == 0
+    print(json.dumps({"case": args.case, "layers": args.layers, "gemvs": len(mats), "calls": args.reps,
+                      "us_per_call_eager": ms * 1e3, "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}),
+          flush=True)
+
+
 def run_case(args):
     """A small profiling case: seeded weights of one shape, rotated over copies (> L2), called reps times."""
     import torch
     if args.case.startswith("q4_chain"):
         return run_chain_case(args)
+    if args.case == "q4_decode_stream":
+        return run_stream_case(args)
 
     import quantized_weight_gemv_gb300 as qg
     from datagen import workloads as W

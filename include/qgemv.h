@@ -190,9 +190,15 @@ int vocab_softcap_argmax(int bits, const uint8_t* lo, const uint8_t* hi, const u
  *        allocation; every completed call leaves it zeroed.  Calls sharing a workspace
  *        must not overlap on the GPU.
  * vocab_softcap_select: vocab_softcap_argmax's soft-capped logits (written to `logits`,
- * required here) followed by qg_logits_select on them, the second launch chained to
- * the first by programmatic dependent launch; ws holds qg_vocab_select_workspace_bytes().
+ * required here) and qg_logits_select's token and logprob over them; ws holds
+ * qg_vocab_select_workspace_bytes().  When allowed is NULL or holds at most
+ * QG_SELECT_FUSED_MAX_ALLOWED IDs and k has the streaming kernel (not QG_FLAG_PLAIN),
+ * one launch does both: each CTA folds the rows it has just produced into the
+ * selection and the last CTA to finish merges; otherwise two launches, the second
+ * chained to the first by programmatic dependent launch.  The token is the same either
+ * way; the log-probability differs only by summation order.
  */
+#define QG_SELECT_FUSED_MAX_ALLOWED 8192
 size_t qg_select_workspace_bytes(void);
 int qg_logits_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token,
                      float* logprob, void* ws, size_t ws_bytes, unsigned flags, void* stream);

@@ -257,6 +257,24 @@ int vocab_softcap_select(int bits, const uint8_t* lo, const uint8_t* hi, const u
     if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
     unsigned char* w = reinterpret_cast<unsigned char*>(ws);
     SelectWorkspace* sw = reinterpret_cast<SelectWorkspace*>(w + sizeof(VocabWorkspace));
+    // one launch: the streaming kernel's selection epilogue (every CTA scans the allowed
+    // list once, hence the bound on its length)
+    if (!(flags & QG_FLAG_PLAIN) && (!allowed || n_allowed <= QG_SELECT_FUSED_MAX_ALLOWED) &&
+        stream_supported(bits, n_vocab, k, 1, EPI_SELECT)) {
+        int rc = check_weights(bits, lo, hi, scale, min, n_vocab, k);
+        if (rc != QG_OK) return rc;
+        if (n_vocab < 1 || !x) return QG_ERR_INVALID_ARG;
+        if (!(softcap == softcap)) return QG_ERR_INVALID_ARG;  // NaN cap
+        if (!aligned16(x) || !aligned16(logits)) return QG_ERR_ALIGNMENT;
+        LaunchCtx lc;
+        rc = resolve(stream, flags, lc);
+        if (rc != QG_OK) return rc;
+        StreamParams sp = {lo,      hi,       scale,   min,     n_vocab, k,      1,        0,
+                           x,       logits,   softcap, nullptr, nullptr, nullptr, allowed, allowed ? n_allowed : 0,
+                           token,   logprob,  sw};
+        rc = launch_stream(sp, bits, EPI_SELECT, lc);
+        if (rc != QG_ERR_UNSUPPORTED) return rc;
+    }
     // 1. the soft-capped logits (its unconstrained argmax goes to the workspace's scratch word)
     int rc = vocab_softcap_argmax(bits, lo, hi, scale, min, n_vocab, k, x, softcap, logits, &sw->scratch_index, w,
                                   sizeof(VocabWorkspace), flags, stream);

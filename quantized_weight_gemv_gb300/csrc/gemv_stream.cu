@@ -9,7 +9,7 @@ bool stream_supported(int bits, int n, int k, int batch, int epi) {
     // int2 LM head of the Gemma WebGPU Engine, "Roadmap")
     if (k != 1536 && (k < 256 || k > 16384 || (k & (k - 1)) != 0)) return false;
     if (batch < 1 || batch > 4) return false;
-    if (epi == EPI_ARGMAX && batch != 1) return false;
+    if ((epi == EPI_ARGMAX || epi == EPI_SELECT) && batch != 1) return false;
     (void)n;
     return true;
 }

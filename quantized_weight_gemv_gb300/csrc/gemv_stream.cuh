@@ -148,6 +148,8 @@ __device__ __forceinline__ void emit_row(const StreamParams& p, long long row, c
 #pragma unroll
         for (int c = 0; c < BC; ++c)
             if (c < p.batch) p.y[(size_t)c * p.n + row] = v[c];
+    } else if constexpr (EPI == EPI_SELECT) {
+        p.y[row] = softcap_apply(v[0], p.softcap);  // folded into the selection at the CTA's end
     } else {
         const float l = softcap_apply(v[0], p.softcap);
         if (p.y) p.y[row] = l;
@@ -410,6 +412,38 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         __shared__ ArgmaxPartial sred[8];
         __shared__ int sflag;
         argmax_finish(bv, bi, p.ws, p.argmax, sred, &sflag);
+    } else if constexpr (EPI == EPI_SELECT) {
+        // Constrained selection over this CTA's rows [r0, r1), which its warps have just
+        // written to y (visible to the whole CTA after the barrier): an online
+        // log-sum-exp (NaN skipped) and the best (value, lowest id) among the allowed ids
+        // that fall in the range, from one pass over the allowed list; the last CTA to
+        // finish merges every CTA's partial.
+        __shared__ SelectPartial sred[8];
+        __shared__ int slast;
+        __syncthreads();
+        float m = -INFINITY, s = 0.0f;
+        float sv = __int_as_float(0x7fc00000);
+        int si = 0x7fffffff;
+        for (long long i = r0 + threadIdx.x; i < r1; i += blockDim.x) {
+            const float l = p.y[i];
+            if (l == l) lse_merge(m, s, l, 1.0f);
+            if (!p.allowed && better(l, (int)i, sv, si)) {
+                sv = l;
+                si = (int)i;
+            }
+        }
+        if (p.allowed) {
+            for (int j = threadIdx.x; j < p.n_allowed; j += blockDim.x) {
+                const long long id = p.allowed[j];
+                if (id < r0 || id >= r1) continue;
+                const float l = p.y[id];
+                if (better(l, (int)id, sv, si)) {
+                    sv = l;
+                    si = (int)id;
+                }
+            }
+        }
+        select_finish(m, s, sv, si, p.sws, p.token, p.logprob, sred, &slast);
     }
 }
 

@@ -40,6 +40,7 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     if (per_sm < 1) per_sm = 1;
     int grid = lc.sm_count * per_sm;
     if (EPI == EPI_ARGMAX && grid > VOCAB_MAX_CTAS) grid = VOCAB_MAX_CTAS;
+    if (EPI == EPI_SELECT && grid > SELECT_MAX_CTAS) grid = SELECT_MAX_CTAS;
     if (grid > p.n) grid = p.n;
     if (grid < 1) grid = 1;
     return launch_kernel(kern, dim3(grid), dim3(W * 32), smem, lc, p);
@@ -63,6 +64,7 @@ int launch_l(const StreamParams& p, const LaunchCtx& lc) {
 template <int BITS>
 int launch_bits(const StreamParams& p, int epi, const LaunchCtx& lc) {
     if (epi == EPI_ARGMAX) return launch_l<BITS, 1, EPI_ARGMAX>(p, lc);
+    if (epi == EPI_SELECT) return launch_l<BITS, 1, EPI_SELECT>(p, lc);
     switch (p.batch) {
         case 1: return launch_l<BITS, 1, EPI_STORE>(p, lc);
         case 2: return launch_l<BITS, 2, EPI_STORE>(p, lc);

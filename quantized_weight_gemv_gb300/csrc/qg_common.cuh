@@ -303,6 +303,97 @@ struct SelectWorkspace {
     SelectPartial part[SELECT_MAX_CTAS];
 };
 
+// (m, s) <- the log-sum-exp pair of the union of two sets, each held as its maximum m
+// and sum of exp(value - m); an empty set is (-inf, 0), an infinite term makes the
+// result (+inf, 1)
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    if (m2 == -INFINITY) return;
+    if (m == INFINITY || m2 == INFINITY) {
+        m = INFINITY;
+        s = 1.0f;
+        return;
+    }
+    if (m == -INFINITY) {
+        m = m2;
+        s = s2;
+        return;
+    }
+    const float M = fmaxf(m, m2);
+    s = s * expf(m - M) + s2 * expf(m2 - M);
+    m = M;
+}
+
+__device__ __forceinline__ void select_warp_reduce(float& m, float& s, float& bv, int& bi) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        lse_merge(m, s, m2, s2);
+        if (better(v2, i2, bv, bi)) {
+            bv = v2;
+            bi = i2;
+        }
+    }
+}
+
+// block-wide merge of (m, s, bv, bi); the result is valid in thread 0
+__device__ __forceinline__ void select_block_reduce(float& m, float& s, float& bv, int& bi, SelectPartial* sred) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    select_warp_reduce(m, s, bv, bi);
+    __syncthreads();
+    if (lane == 0) sred[wid] = SelectPartial{m, s, bv, bi};
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < nw; ++w) {
+            lse_merge(m, s, sred[w].m, sred[w].s);
+            if (better(sred[w].bv, sred[w].bi, bv, bi)) {
+                bv = sred[w].bv;
+                bi = sred[w].bi;
+            }
+        }
+    }
+}
+
+// This CTA's partial (each thread's share in m, s, bv, bi) goes to ws; the last CTA to
+// finish merges every CTA's partial, writes the selected id (-1 when nothing allowed
+// is selectable) and bv - log-sum-exp, and re-arms the counter.  No CTA waits on
+// another.  Called by all threads; gridDim.x <= SELECT_MAX_CTAS.
+__device__ __forceinline__ void select_finish(float m, float s, float bv, int bi, SelectWorkspace* ws,
+                                              int32_t* token, float* logprob, SelectPartial* sred /* [8] */,
+                                              int* slast) {
+    select_block_reduce(m, s, bv, bi, sred);
+    if (threadIdx.x == 0) {
+        ws->part[blockIdx.x] = SelectPartial{m, s, bv, bi};
+        __threadfence();
+        *slast = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!*slast) return;
+    __threadfence();
+    m = -INFINITY;
+    s = 0.0f;
+    bv = __int_as_float(0x7fc00000);
+    bi = 0x7fffffff;
+    for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+        const float cm = __ldcg(&ws->part[c].m), cs = __ldcg(&ws->part[c].s);
+        const float cv = __ldcg(&ws->part[c].bv);
+        const int ci = __ldcg(&ws->part[c].bi);
+        lse_merge(m, s, cm, cs);
+        if (better(cv, ci, bv, bi)) {
+            bv = cv;
+            bi = ci;
+        }
+    }
+    select_block_reduce(m, s, bv, bi, sred);
+    if (threadIdx.x == 0) {
+        const bool found = bi != 0x7fffffff;
+        *token = found ? bi : -1;
+        *logprob = found ? bv - (m + logf(s)) : __int_as_float(0x7fc00000);
+        ws->counter = 0u;
+    }
+}
+
 // Block-wide (value, index) reduction, then the last CTA to finish reduces every
 // CTA's partial, writes the index and re-arms the counter.  No CTA waits on another.
 // Called by all threads of the block.

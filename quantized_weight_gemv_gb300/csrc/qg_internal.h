@@ -8,7 +8,9 @@
 
 namespace qg {
 
-enum : int { EPI_STORE = 0, EPI_ARGMAX = 1 };
+// Epilogue of the single-matrix kernels: plain store; soft-cap + argmax; soft-cap +
+// constrained selection (log-sum-exp and best allowed id, stream kernel only).
+enum : int { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_SELECT = 2 };
 
 // per-column shared-memory stride of a quantised activation (16-byte aligned)
 __host__ __device__ constexpr int xq_stride(int nb) { return (xq_bytes(nb) + 15) & ~15; }
@@ -39,6 +41,12 @@ struct StreamParams {
     int32_t* argmax;
     VocabWorkspace* ws;
     unsigned int* err;  // device error word
+    // EPI_SELECT: allowed ids (null: all), the selected id and its log-probability
+    const int32_t* allowed;
+    int n_allowed;
+    int32_t* token;
+    float* logprob;
+    SelectWorkspace* sws;
 };
 
 struct CqParams {

@@ -12,55 +12,6 @@
 
 namespace qg {
 
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
-    if (m2 == -INFINITY) return;
-    if (m == INFINITY || m2 == INFINITY) {  // an infinite term: log-sum-exp = +inf
-        m = INFINITY;
-        s = 1.0f;
-        return;
-    }
-    if (m == -INFINITY) {
-        m = m2;
-        s = s2;
-        return;
-    }
-    const float M = fmaxf(m, m2);
-    s = s * expf(m - M) + s2 * expf(m2 - M);
-    m = M;
-}
-
-__device__ __forceinline__ void select_warp_reduce(float& m, float& s, float& bv, int& bi) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-        lse_merge(m, s, m2, s2);
-        if (better(v2, i2, bv, bi)) {
-            bv = v2;
-            bi = i2;
-        }
-    }
-}
-
-// block-wide merge of (m, s, bv, bi); the result is valid in thread 0
-__device__ __forceinline__ void select_block_reduce(float& m, float& s, float& bv, int& bi, SelectPartial* sred) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    select_warp_reduce(m, s, bv, bi);
-    __syncthreads();
-    if (lane == 0) sred[wid] = SelectPartial{m, s, bv, bi};
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < nw; ++w) {
-            lse_merge(m, s, sred[w].m, sred[w].s);
-            if (better(sred[w].bv, sred[w].bi, bv, bi)) {
-                bv = sred[w].bv;
-                bi = sred[w].bi;
-            }
-        }
-    }
-}
-
 __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ logits, int n,
                                                      const int32_t* __restrict__ allowed, int n_allowed,
                                                      int32_t* token, float* logprob, SelectWorkspace* ws) {
@@ -107,36 +58,7 @@ __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ l
             bi = (int)id;
         }
     }
-    select_block_reduce(m, s, bv, bi, sred);
-    if (threadIdx.x == 0) {
-        ws->part[blockIdx.x] = SelectPartial{m, s, bv, bi};
-        __threadfence();
-        last = atomicAdd(&ws->counter, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    m = -INFINITY;
-    s = 0.0f;
-    bv = __int_as_float(0x7fc00000);
-    bi = 0x7fffffff;
-    for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
-        const float cm = __ldcg(&ws->part[c].m), cs = __ldcg(&ws->part[c].s);
-        const float cv = __ldcg(&ws->part[c].bv);
-        const int ci = __ldcg(&ws->part[c].bi);
-        lse_merge(m, s, cm, cs);
-        if (better(cv, ci, bv, bi)) {
-            bv = cv;
-            bi = ci;
-        }
-    }
-    select_block_reduce(m, s, bv, bi, sred);
-    if (threadIdx.x == 0) {
-        const bool found = bi != 0x7fffffff;
-        *token = found ? bi : -1;
-        *logprob = found ? bv - (m + logf(s)) : __int_as_float(0x7fc00000);
-        ws->counter = 0u;
-    }
+    select_finish(m, s, bv, bi, ws, token, logprob, sred, &last);
 }
 
 int launch_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token, float* logprob,

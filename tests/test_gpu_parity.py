@@ -100,6 +100,21 @@ def test_gemv_random(bits, n, k, flags):
     assert_close(y, oracle.gemv(w, x))
 
 
+@pytest.mark.parametrize("n,k", [(304 * 23 + 7, 1536), (304 * 37 + 5, 1024), (304 * 17 + 3, 2048),
+                                 (304 * 9 + 1, 4096)])
+def test_q2_stage_tails(n, k):
+    """Q2 at one column streams 512-block stages (10 rows of k = 1536, 16 / 8 / 4 rows of
+    k = 1024 / 2048 / 4096): with 2 CTAs per SM on 152 SMs each CTA here holds several
+    full stages and a ragged last one.  GEMV and the soft-cap + argmax epilogue."""
+    w = datagen.make_quantized(2, 31 * n + k, n, k)
+    x = datagen.normal_f32(31 * n + k, 1, k)
+    wd = dev_w(w)
+    ref = oracle.gemv(w, x)
+    for flags in (0, qg.QG_FLAG_PDL):
+        assert_close(gpu_gemv(wd, x, flags), ref)
+    _vocab_check(w, x, 30.0, 0)
+
+
 @pytest.mark.parametrize("bits", [4, 6])
 def test_gemv_special_activations(bits):
     n, k = 64, 2048
@@ -430,9 +445,12 @@ def test_logits_select_nothing_allowed():
     assert int(tok.item()) == -1 and np.isnan(float(lp.item()))
 
 
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits", [2, 4, 6])
 def test_vocab_softcap_select(bits):
-    n, k = 40000, 2048
+    """One launch (the stream kernel's selection epilogue) for no list or up to
+    QG_SELECT_FUSED_MAX_ALLOWED ids, two launches for a longer list (here 20000 ids,
+    unsorted, with duplicates and out-of-range ids) or the plain kernel."""
+    n, k = 40000, 1536 if bits == 2 else 2048
     w = datagen.make_quantized(bits, 66, n, k)
     x = datagen.normal_f32(66, 1, k)
     wd = dev_w(w)
@@ -440,9 +458,10 @@ def test_vocab_softcap_select(bits):
     ref_l = oracle.softcap(oracle_gemv_par(w, x), 30.0)
     rng = np.random.default_rng(67)
     ws = qg.vocab_select_workspace(DEV)
-    for allowed in (None, np.sort(rng.choice(n, size=500, replace=False)).astype(np.int32)):
+    long_list = np.concatenate([rng.integers(0, n, 19990), [-3, n, n + 5, 7, 7, 7, 11, 0, 1, 2]]).astype(np.int32)
+    for allowed in (None, np.sort(rng.choice(n, size=500, replace=False)).astype(np.int32), long_list):
         at = None if allowed is None else torch.from_numpy(allowed).to(DEV)
-        for flags in (0, qg.QG_FLAG_PDL):
+        for flags in (0, qg.QG_FLAG_PDL, qg.QG_FLAG_PLAIN):
             logits, tok, lp = qg.vocab_softcap_select(bits, wd["lo"], wd.get("hi"), wd["scale"], wd["min"], xt, 30.0,
                                                       allowed=at, ws=ws, flags=flags)
             l = logits.cpu().numpy()
@@ -451,7 +470,7 @@ def test_vocab_softcap_select(bits):
             own_tok, _ = oracle.select(l.astype(np.float64), allowed)
             assert int(tok.item()) == own_tok
             ref_tok, ref_lp = oracle.select(ref_l, allowed)
-            cand = ref_l if allowed is None else ref_l[allowed]
+            cand = ref_l if allowed is None else ref_l[np.unique(allowed[(allowed >= 0) & (allowed < n)])]
             top2 = np.sort(cand)[-2:]
             if top2[1] - top2[0] > 2 * TOL * max(abs(top2[1]), float(np.sqrt(np.mean(ref_l ** 2)))):
                 assert int(tok.item()) == ref_tok

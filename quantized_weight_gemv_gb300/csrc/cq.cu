@@ -6,8 +6,11 @@
 // transform of the weights is never materialised.  "TypeGPU": one 32-lane group
 // per output row.  "Custom backend": an optional contiguous row range.
 //
-// Each CTA transforms x itself: a warp owns a group of G = 32*J values, lane l
-// holding elements J*l .. J*l+J-1.  The butterflies over the low log2(J) index
+// Each warp first pulls the packed indices of its first row into L1 and loads that
+// row's scale (weights: under programmatic dependent launch they are read before the
+// preceding kernel has finished), so that their latency overlaps the transform.  Each
+// CTA transforms x itself: a warp owns a group of G = 32*J values, lane l holding
+// elements J*l .. J*l+J-1.  The butterflies over the low log2(J) index
 // bits run in registers, those over the lane bits through __shfl_xor_sync.  The
 // result is kept in shared memory transposed (element J*l + j at j*32 + l), so
 // that in the dot loop lane l reads its J values without bank conflicts.
@@ -59,10 +62,21 @@ __global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
     __shared__ float scb[16];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int ngroups = p.k / G;
+    const size_t row_bytes = (size_t)(p.k >> 1);
+
+    // the warp's first row: index lines prefetched into L1, row scale loaded, before the wait
+    const int j0 = blockIdx.x * 8 + wid;
+    unsigned short scale0 = 0;
+    if (j0 < p.row_count) {
+        const uint8_t* rp = p.idx + (size_t)(p.row_start + j0) * row_bytes;
+        for (size_t off = (size_t)lane * 128; off < row_bytes; off += 32 * 128)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(rp + off));
+        scale0 = p.row_scale[p.row_start + j0];
+    }
+    if (threadIdx.x < 16) scb[threadIdx.x] = half_bits_to_float(p.codebook[threadIdx.x]);
 
     pdl_wait();
     if (threadIdx.x == 0) pdl_launch_dependents();
-    if (threadIdx.x < 16) scb[threadIdx.x] = half_bits_to_float(p.codebook[threadIdx.x]);
 
     for (int g = wid; g < ngroups; g += 8) {
         float v[J];
@@ -92,8 +106,7 @@ __global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
     }
     __syncthreads();
 
-    const size_t row_bytes = (size_t)(p.k >> 1);
-    for (int j = blockIdx.x * 8 + wid; j < p.row_count; j += gridDim.x * 8) {
+    for (int j = j0; j < p.row_count; j += gridDim.x * 8) {
         const int r = p.row_start + j;
         const uint8_t* rp = p.idx + (size_t)r * row_bytes;
         float acc = 0.0f;
@@ -108,7 +121,7 @@ __global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
             }
         }
         acc = warp_sum(acc);
-        if (lane == 0) p.y[j] = half_bits_to_float(p.row_scale[r]) * acc;
+        if (lane == 0) p.y[j] = half_bits_to_float(j == j0 ? scale0 : p.row_scale[r]) * acc;
     }
 }
 

@@ -5,18 +5,19 @@
 // README, "Performance"; genie-ai-runtime, "The decode arc").  The kernel is shaped
 // for that:
 //  * CTA b owns the contiguous rows [b*n/G, (b+1)*n/G) of the matrix (G = grid).
-//  * A stage is 256 consecutive blocks of 32 weights in row-major order: R = 256/nb
-//    whole rows when nb = k/32 <= 256, else one 256-block part of a row.  Each
-//    stage is one contiguous span per plane (codes, [hi,] scale, min), fetched by
-//    one cp.async.bulk per plane, completion tracked by an mbarrier.
+//  * A stage is SB consecutive blocks of 32 weights in row-major order (SB = 256, or
+//    512 for Q2 at one column: the same 5 KB): R = SB/nb whole rows when nb = k/32 <=
+//    SB, else one SB-block part of a row.  Each stage is one contiguous span per plane
+//    (codes, [hi,] scale, min), fetched by one cp.async.bulk per plane, completion
+//    tracked by an mbarrier.
 //  * Warp w of the CTA owns units w, w+W, w+2W, ... (a unit is a stage's rows, or
-//    one whole row of nb/256 stages when nb > 256) and keeps D stages of its own in
+//    one whole row of nb/SB stages when nb > SB) and keeps D stages of its own in
 //    flight in D private slots.  Its lane 0 issues the copies.  The first D are
 //    issued before griddepcontrol.wait, so under programmatic dependent launch the
 //    weight stream overlaps the tail of the preceding kernel.
 //  * A warp moves a landed stage from shared memory into registers, refills the
 //    slot with its next stage at once, and only then computes: lane l takes blocks
-//    l + 32j (j < 8) of the stage, dots each with the int8 activation by dp4a over
+//    l + 32j (j < SB/32) of the stage, dots each with the int8 activation by dp4a over
 //    nibbles unpacked from 32-bit words (genie-ai-runtime, "The decode arc": dp4a
 //    int8 MMVQ "instead of dequant-to-fp"; its uint32 fast path for the dequant
 //    loop), applies the fp32 block combine s_b * (scale * D + min * S_b), and
@@ -26,6 +27,9 @@
 //  * A lane's block positions are the same in every stage, so for short rows its
 //    activation words live in registers; for long rows they are read from shared
 //    memory, stored as split halves so that the 128-bit reads are conflict-free.
+//  * Epilogues: plain store; soft-cap + argmax; soft-cap + constrained selection (each
+//    CTA folds its own rows into a log-sum-exp and an allowed best once they are
+//    written).  Both reductions end in a last-arriver merge, no CTA waits on another.
 //  * Every wait is bounded (mbarrier try_wait against %globaltimer); on expiry the
 //    kernel ORs a code into the library's device error word and stops.
 #pragma once
@@ -35,8 +39,8 @@
 namespace qg {
 namespace stream {
 
-constexpr int SBW = 256;  // blocks per stage
-constexpr int JPL = 8;    // blocks per lane per stage
+constexpr int SBW = 256;  // blocks per stage (the grouped and chain kernels; the base size here)
+constexpr int JPL = 8;    // blocks per lane per stage of SBW blocks
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 

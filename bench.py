@@ -312,13 +312,14 @@ def time_eager(fn, stream, reps, warm=3):
 
 def ch_launches(stages, flags):
     """Kernel launches per call of the decode chain: the persistent kernel is one; the
-    per-phase mode is one per phase whose input is short (q/k/v, o, gate/up: 2048
-    values) and two for the down projection's 16384-value input."""
+    per-phase mode is one per phase: the short inputs (q/k/v, o, gate/up: 2048 values)
+    are quantised by every CTA, and the down projection's 16384-value input, the whole
+    gate output of the phase before, is quantised by the gate/up launch itself."""
     import quantized_weight_gemv_gb300 as qg
 
     if flags & qg.QG_FLAG_CHAIN_PERSISTENT:
         return 1
-    return sum(2 if i % 4 == 3 else 1 for i in range(len(stages)))
+    return len(stages)
 
 
 def decode_chain_rows(mats, n_layers, total_bytes, stream, reps):

@@ -280,12 +280,15 @@ int qgemv_grouped_noalloc(int bits, const qg_gemv_desc* descs, int count, unsign
  *   values.  Across phases buffers may be reused freely.
  *   ws : device workspace of at least qg_chain_workspace_bytes(...) bytes, 16-byte
  *        aligned; its first QG_CHAIN_CTL_BYTES bytes are zero-filled once after
- *        allocation and every call that completes leaves them zero.  Calls sharing a workspace must not
- *        overlap on the GPU.
+ *        allocation and every call that completes leaves them zero.  Calls sharing a
+ *        workspace must not overlap on the GPU.
  * Default: each phase runs as qgemv_grouped's launches, phase f+1 chained to phase f
  * by programmatic dependent launch (QG_FLAG_PDL applies to the first phase); a phase
  * whose distinct inputs are short (6144 values in all) is one launch whose CTAs
- * quantise the inputs themselves.  With QG_FLAG_CHAIN_PERSISTENT: one cooperative
+ * quantise the inputs themselves, and a phase whose long inputs are all whole outputs
+ * of the phase before (x == that y, k == its n) is one launch too: each CTA of the
+ * phase before, its rows of such an output aligned to whole blocks of 32, quantises
+ * them into the workspace once they are stored.  With QG_FLAG_CHAIN_PERSISTENT: one cooperative
  * launch, one CTA per SM, whose producer warp streams every phase's weights through
  * a bulk-copy ring that runs ahead across phase boundaries, with a grid-wide barrier
  * between phases.  That launch starts after the preceding work on the stream has

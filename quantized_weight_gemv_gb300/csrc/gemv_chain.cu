@@ -149,6 +149,25 @@ __device__ bool wait_empty(uint64_t* bar, uint32_t parity, const volatile int* a
     }
 }
 
+// Consumer: wait until the producer has issued at least n + 1 tiles (bounded; false when
+// the CTA is stopping or after WAIT_LIMIT_NS).  A tile is waited for on its slot's full
+// barrier only once issued: the producer issues tile n after tile n - NS was read, so the
+// barrier has then completed tile n - NS's phase and a parity wait cannot take that
+// earlier phase for tile n's.  Without this a warp whose next tile lies two ring laps
+// ahead of the oldest pending one (15 warps, two tiles a unit, 16 slots) would pass on
+// the parity of the phase two laps back.
+__device__ bool wait_issued(const volatile int* issued, int n, const volatile int* abort_flag) {
+    if (*issued > n) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (*issued > n) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+
 template <int BITS>
 __device__ __forceinline__ void issue_tile(const CDesc& d, int ul, int part, unsigned char* slot, uint64_t* bar,
                                            uint64_t pol) {
@@ -251,6 +270,7 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CP
     using SL = stream::Slot<BITS>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ volatile int s_abort;
+    __shared__ volatile int s_issued;  // tiles the producer has issued
     __shared__ Range s_range[QG_MAX_GROUP];  // this CTA's share of every phase
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NS = 1 << p.log2slots;
@@ -262,6 +282,7 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CP
 
     if (threadIdx.x == 0) {
         s_abort = 0;
+        s_issued = 0;
         for (int i = 0; i < NS; ++i) {
             stream::mbar_init(&full[i], 1);
             stream::mbar_init(&empty[i], 1);
@@ -321,6 +342,11 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CP
             if (!stop && lane < cnt)
                 issue_tile<BITS>(p.d[my_di], my_ul, my_part, ring + (size_t)slot * SL::BYTES, &full[slot], pol);
             if (!stop) n += cnt;
+            __syncwarp();
+            if (lane == 0 && !stop) {  // publish the batch to the consumers
+                __threadfence_block();
+                s_issued = n;
+            }
         }
         // copies in flight land before the CTA exits (the last NS issued)
         if (lane == 0) {
@@ -366,7 +392,9 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CP
                     const int n = base + tile_index(d, u, part) - r.t0;
                     const int slot = n & (NS - 1);
                     // all lanes poll; the decision is taken together so that the warp stays converged
-                    if (!__all_sync(0xffffffffu, stream::mbar_wait(&full[slot], (uint32_t)((n >> LS) & 1)))) {
+                    const bool ready = wait_issued(&s_issued, n, &s_abort);
+                    __threadfence_block();
+                    if (!__all_sync(0xffffffffu, ready && stream::mbar_wait(&full[slot], (uint32_t)((n >> LS) & 1)))) {
                         if (lane == 0) atomicOr(p.err, ERR_WAIT_FULL);
                         s_abort = 1;
                         bad = true;
@@ -429,35 +457,78 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CP
 
 }  // namespace chain
 
-size_t chain_workspace_bytes(const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase) {
-    (void)count;
-    size_t mx = 0;
+// Workspace of the per-phase mode after the control words: three regions of A bytes,
+// the images of a phase that quantises its own inputs and two (by phase parity) for
+// images that a phase produces for the next one.
+static size_t chain_image_region(const qg_gemv_desc* descs, const int* phase_sizes, int nphase) {
+    size_t A = 0;
     int off = 0;
     for (int f = 0; f < nphase; ++f) {
         const size_t b = grouped_workspace_bytes(descs + off, phase_sizes[f]);
-        if (b > mx) mx = b;
+        if (b > A) A = b;
         off += phase_sizes[f];
     }
-    return (size_t)QG_CHAIN_CTL_BYTES + mx;
+    return (A + 15) & ~(size_t)15;
+}
+
+size_t chain_workspace_bytes(const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase) {
+    (void)count;
+    return (size_t)QG_CHAIN_CTL_BYTES + 3 * chain_image_region(descs, phase_sizes, nphase);
+}
+
+// Whether the images of phase C (nc descriptors) can come from phase P: C takes the
+// two-launch form (its inputs are long), and every active descriptor of C reads the
+// whole output of an active descriptor of P (x == y, k == n, n a multiple of 32).  On
+// success outs[0..*nout) name the producers with C's image offsets (in C's workspace
+// layout, based at img).
+static bool plan_produced(const qg_gemv_desc* P, int np, const qg_gemv_desc* C, int nc, unsigned char* img,
+                          GroupedOut* outs, int* nout) {
+    *nout = 0;
+    if (grouped_fuses(C, nc)) return false;
+    size_t off = 0;
+    for (int j = 0; j < nc; ++j) {
+        if (C[j].n == 0) continue;
+        int i = 0;
+        while (i < np && !(P[i].n > 0 && P[i].n % 32 == 0 && P[i].y == C[j].x && P[i].n == C[j].k)) ++i;
+        if (i == np || *nout == GROUPED_MAX_OUT) return false;
+        outs[*nout] = GroupedOut{i, img + off};
+        ++*nout;
+        off += (size_t)xq_stride(C[j].k >> 5);
+    }
+    return *nout > 0;
 }
 
 int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase,
                  unsigned char* ws, const LaunchCtx& lc) {
     using namespace chain;
     (void)count;
-    if (!(lc.flags & QG_FLAG_CHAIN_PERSISTENT)) {  // one grouped launch (pair) per phase
+    if (!(lc.flags & QG_FLAG_CHAIN_PERSISTENT)) {
+        // One grouped launch (pair) per phase.  A phase with long inputs that are whole
+        // outputs of the phase before takes its images from that phase, which quantises
+        // its outputs block by block as they complete: one launch instead of two.
+        const size_t A = chain_image_region(descs, phase_sizes, nphase);
+        unsigned char* own = ws + QG_CHAIN_CTL_BYTES;
+        unsigned char* produced[2] = {own + A, own + 2 * A};
         int off = 0;
-        bool launched = false;
+        bool launched = false, ready = false;
         for (int f = 0; f < nphase; ++f) {
             LaunchCtx l2 = lc;
             if (launched) l2.flags |= QG_FLAG_PDL;
             bool any = false;
             for (int i = off; i < off + phase_sizes[f]; ++i) any = any || descs[i].n > 0;
+            GroupedOut outs[GROUPED_MAX_OUT];
+            int nout = 0;
+            const bool next_ready =
+                any && f + 1 < nphase &&
+                plan_produced(descs + off, phase_sizes[f], descs + off + phase_sizes[f], phase_sizes[f + 1],
+                              produced[(f + 1) & 1], outs, &nout);
             if (any) {
-                const int rc = launch_grouped(bits, descs + off, phase_sizes[f], ws + QG_CHAIN_CTL_BYTES, l2, true);
+                const int rc = launch_grouped(bits, descs + off, phase_sizes[f], ready ? produced[f & 1] : own, l2,
+                                              true, outs, next_ready ? nout : 0, ready);
                 if (rc != QG_OK) return rc;
                 launched = true;
             }
+            ready = next_ready;
             off += phase_sizes[f];
         }
         return QG_OK;

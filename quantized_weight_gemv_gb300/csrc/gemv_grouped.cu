@@ -41,12 +41,23 @@ struct GDesc {
     int qb_prefix;     // activation blocks of the descriptors before
     int ws_off;        // byte offset of this descriptor's activation image in the workspace
                        // (SMX: in the kernel's shared-memory image area)
+    int qalign;        // units per 32 rows when its output image is produced here, else 1
 };
 
 struct GInput {  // a distinct activation of an SMX group and its shared-memory image
     const float* x;
     int k;
     int off;
+};
+
+// An activation image that the kernel produces from one descriptor's output for the
+// next launch (the chain's long-input phases).  The CTAs' unit ranges are aligned to
+// whole blocks of 32 rows inside a producing descriptor, so each CTA quantises the
+// blocks of its own rows once they are stored.
+struct GOut {
+    int desc;            // producing descriptor
+    int nq;              // blocks of 32 outputs (its n / 32)
+    unsigned char* img;  // the image (xq_view layout for nq blocks)
 };
 
 struct GParams {
@@ -59,6 +70,8 @@ struct GParams {
     unsigned char* ws;
     int nin;        // SMX: distinct activations, quantised by every CTA after griddepcontrol.wait
     int img_bytes;  // SMX: bytes of their shared-memory images
+    int nout;  // images produced for the next launch
+    GOut out[GROUPED_MAX_OUT];
     GDesc d[QG_MAX_GROUP];
     GInput in[QG_MAX_GROUP];
 };
@@ -124,12 +137,15 @@ struct Cursor {
     }
 };
 
-// first global unit whose first stage is at or after global stage x
+// first global unit whose first stage is at or after global stage x; inside a
+// descriptor whose output image is produced, rounded up to a whole block of 32 rows
+// (monotone in x, so consecutive CTAs' ranges still tile the units)
 __device__ __forceinline__ int unit_at_stage(const GParams& p, int x) {
     if (x >= p.total_stages) return p.total_units;
     const int di = find_desc(p, x, [](const GDesc& d) { return d.stage_prefix; });
     const GDesc& d = p.d[di];
-    const int local = (x - d.stage_prefix + d.parts - 1) / d.parts;
+    int local = (x - d.stage_prefix + d.parts - 1) / d.parts;
+    if (d.qalign > 1) local = min((local + d.qalign - 1) / d.qalign * d.qalign, d.units);
     return d.unit_prefix + local;
 }
 
@@ -320,6 +336,36 @@ __global__ void __launch_bounds__(256, MINB) grouped_gemv_kernel(const __grid_co
         }
         cc.advance(p);
     }
+
+    if (p.nout > 0) {
+        // Images for the next launch: this CTA's rows of a producing descriptor are whole
+        // blocks of 32 (aligned ranges), visible to the whole CTA after the barrier; a
+        // warp per block quantises them exactly as the activation quantisation kernel does.
+        __syncthreads();
+        for (int o = 0; o < p.nout; ++o) {
+            const GOut& out = p.out[o];
+            const GDesc& d = p.d[out.desc];
+            const int R = d.log2nb >= 8 ? 1 : 256 >> d.log2nb;
+            const int ua = max(u_begin, d.unit_prefix) - d.unit_prefix;
+            const int ub = min(u_end, d.unit_prefix + d.units) - d.unit_prefix;
+            if (ua >= ub) continue;
+            const int qb = min(ub * R, d.n) >> 5;
+            for (int q = ((ua * R) >> 5) + warp; q < qb; q += 8) {
+                float s;
+                int S;
+                const int code = quantize_lane(__ldcg(d.y + 32 * q + lane), s, S);
+                const XqView v = xq_view(out.img, out.nq);
+                if (lane < 16)
+                    v.lo[16 * q + lane] = (int8_t)code;
+                else
+                    v.hi[16 * q + lane - 16] = (int8_t)code;
+                if (lane == 0) {
+                    v.s[q] = s;
+                    v.S[q] = (float)S;
+                }
+            }
+        }
+    }
 }
 
 // fused form: distinct activations of at most this many image bytes (k <= 6144 in total)
@@ -339,16 +385,35 @@ size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count) {
     return off;
 }
 
+// distinct activations (by x and k) of the active descriptors and their image bytes
+static int distinct_image_bytes(const qg_gemv_desc* descs, int count) {
+    int bytes = 0;
+    for (int i = 0; i < count && bytes <= grouped::SMX_MAX_IMAGE; ++i) {
+        if (descs[i].n == 0) continue;
+        bool seen = false;
+        for (int j = 0; j < i && !seen; ++j)
+            seen = descs[j].n > 0 && descs[j].x == descs[i].x && descs[j].k == descs[i].k;
+        if (!seen) bytes += xq_stride(descs[i].k >> 5);
+    }
+    return bytes;
+}
+
+bool grouped_fuses(const qg_gemv_desc* descs, int count) {
+    return distinct_image_bytes(descs, count) <= grouped::SMX_MAX_IMAGE;
+}
+
 int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc,
-                   bool fuse) {
+                   bool fuse, const GroupedOut* outs, int nout, bool images_ready) {
     using namespace grouped;
     static_assert(sizeof(GParams) < 32000, "grouped parameters must fit the kernel parameter space");
     GParams p;
     memset(&p, 0, sizeof(p));
     long long units = 0, stages = 0, qblocks = 0, off = 0;
     int m = 0;
+    int internal[QG_MAX_GROUP];  // caller's descriptor index -> p.d index (-1: empty)
     for (int i = 0; i < count; ++i) {
         const qg_gemv_desc& s = descs[i];
+        internal[i] = s.n == 0 ? -1 : m;
         if (s.n == 0) continue;
         const int nb = s.k >> 5;
         int l = 0;
@@ -362,6 +427,7 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
         d.y = s.y;
         d.n = s.n;
         d.log2nb = l;
+        d.qalign = 1;
         const int R = nb >= 256 ? 1 : 256 / nb;
         d.parts = nb > 256 ? nb / 256 : 1;
         d.units = nb >= 256 ? s.n : (s.n + R - 1) / R;
@@ -382,12 +448,19 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
     p.total_qblocks = (int)qblocks;
     p.err = lc.err;
     p.ws = ws;
+    for (int o = 0; o < nout && o < GROUPED_MAX_OUT; ++o) {
+        const int di = outs[o].desc;
+        if (di < 0 || di >= count || internal[di] < 0 || descs[di].n % 32 != 0) return QG_ERR_INVALID_ARG;
+        GDesc& d = p.d[internal[di]];
+        d.qalign = 32 / (d.log2nb >= 8 ? 1 : 256 >> d.log2nb);  // units per 32 rows
+        p.out[p.nout++] = GOut{internal[di], descs[di].n / 32, outs[o].img};
+    }
 
     // Fused form: when the group's distinct activations (by x and k) are short, every
     // CTA quantises them itself into shared memory after griddepcontrol.wait and the
     // quantisation launch is skipped - one dependent launch instead of two.
     bool smx = false;
-    if (fuse) {
+    if (fuse && !images_ready) {
         int ni = 0, ioff = 0, woff[QG_MAX_GROUP];
         for (int i = 0; i < m && ioff <= SMX_MAX_IMAGE; ++i) {
             const int k = 32 << p.d[i].log2nb;
@@ -410,8 +483,8 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
         }
     }
 
-    // 1. activations
-    if (!smx) {
+    // 1. activations (unless the preceding launch produced them)
+    if (!smx && !images_ready) {
         long long qgrid = (qblocks + 7) / 8;
         if (qgrid > lc.sm_count * 16) qgrid = lc.sm_count * 16;
         int rc = launch_kernel(grouped_quantize_kernel, dim3((unsigned)qgrid), dim3(256), 0, lc, p);
@@ -449,7 +522,7 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
     long long grid = (long long)lc.sm_count * grid_per_sm;
     if (grid > units) grid = units;
     LaunchCtx lc2 = lc;
-    if (!smx) lc2.flags |= QG_FLAG_PDL;
+    if (!smx && !images_ready) lc2.flags |= QG_FLAG_PDL;
     return launch_kernel(kern, dim3((unsigned)grid), dim3(256), smem, lc2, p);
 }
 

@@ -104,9 +104,23 @@ size_t mma_workspace_bytes(int k, int batch);
 // ws: the activation image (mma_workspace_bytes), or null to quantise in every CTA
 int launch_mma(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc);
 size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count);
-// fuse: allow the one-launch form (activations quantised in every CTA) when they are short
+// Whether launch_grouped(..., fuse = true) takes the one-launch form for this group:
+// its distinct activations (by x and k) are short enough to be quantised in every CTA.
+bool grouped_fuses(const qg_gemv_desc* descs, int count);
+// An activation image that a grouped launch produces for the next launch from the
+// output of its descriptor `desc` (index into its descs array, n % 32 == 0): written
+// to img in the workspace image layout for k = n.
+constexpr int GROUPED_MAX_OUT = 4;
+struct GroupedOut {
+    int desc;
+    unsigned char* img;
+};
+// fuse: allow the one-launch form (activations quantised in every CTA) when they are
+// short.  outs/nout: images to produce for the next launch.  images_ready: the
+// workspace images were produced by the preceding launch (no quantisation launch;
+// the GEMV kernel is chained to that launch by the caller's QG_FLAG_PDL).
 int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char* ws, const LaunchCtx& lc,
-                   bool fuse = false);
+                   bool fuse = false, const GroupedOut* outs = nullptr, int nout = 0, bool images_ready = false);
 size_t chain_workspace_bytes(const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase);
 // ws: the caller's chain workspace (control words first); arguments already validated
 int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase_sizes, int nphase,

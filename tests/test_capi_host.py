@@ -199,7 +199,9 @@ def test_chain_validation(lib):
     d1 = D(W, None, W, W, Y1, Y2, 2048, 2048)       # phase 1 reads phase 0's output
     keep, vp, ps_keep, ps = _chain_args([d0, d1], [1, 1])
     need = lib.qg_chain_workspace_bytes(vp, 2, ps, 2)
-    assert need == qg.QG_CHAIN_CTL_BYTES + 40 * 64    # control words + the largest phase's activation image
+    # control words and three regions of the largest phase's activation images (a phase's
+    # own, and two for images produced by the phase before)
+    assert need == qg.QG_CHAIN_CTL_BYTES + 3 * 40 * 64
     f = lib.qgemv_chain
     assert f(5, vp, 2, ps, 2, A16, need, 0, None) == qg.QG_ERR_UNSUPPORTED
     assert f(4, vp, 0, None, 0, None, 0, 0, None) == qg.QG_OK
@@ -231,7 +233,7 @@ def test_chain_validation(lib):
     assert f(4, vp4, 3, ps4, 1, A16, big, 0, None) == qg.QG_ERR_UNSUPPORTED
     shared = [D(W, None, W, W, X, Y1 + i * 0x1000, 8, 16384) for i in range(3)]  # one input, three GEMVs
     _, vp5, _, ps5 = _chain_args(shared, [3])
-    assert lib.qg_chain_workspace_bytes(vp5, 3, ps5, 1) == qg.QG_CHAIN_CTL_BYTES + 3 * 40 * 512
+    assert lib.qg_chain_workspace_bytes(vp5, 3, ps5, 1) == qg.QG_CHAIN_CTL_BYTES + 3 * (3 * 40 * 512)
     # descriptor rules as for qgemv_grouped
     for bad, rc in ((D(W, None, W, W, X, Y1, 8, 1536), qg.QG_ERR_UNSUPPORTED),
                     (D(W, None, W, W, X + 4, Y1, 8, 2048), qg.QG_ERR_ALIGNMENT),

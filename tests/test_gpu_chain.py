@@ -56,6 +56,40 @@ def test_chain_small(bits, flags):
         assert_close(y.cpu().numpy().astype(np.float64), r)
 
 
+PRODUCED = [  # (n, k, src); phases [3, 3, 1, 2]
+    (8192, 1024, -1), (16384, 2048, -2), (300, 1024, -1),  # 0-2: short inputs
+    (8192, 8192, 0), (1024, 16384, 1), (777, 8192, 0),    # 3-5: long inputs, all outputs of phase 0
+    (2048, 8192, 3),                                       # 6: long input, output of phase 1
+    (1024, 2048, 6), (512, 16384, 1),                      # 7-8: one input from phase 2, one from phase 0
+]
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_chain_produced_images(bits):
+    """Per-phase mode: a phase with long inputs that are whole outputs of the phase before
+    takes its activation images from that phase, whose CTAs (their rows aligned to whole
+    blocks of 32) quantise their own rows once stored.  Phase 1 takes three images from phase 0 (two of them of
+    one output), phase 2 one from phase 1 (a phase whose own images were produced), phase 3
+    quantises for itself (one input comes from two phases back).  Against the oracle,
+    identical over repeated calls on one workspace, and bit-identical to the persistent
+    kernel, which quantises every input itself."""
+    ext = [datagen.normal_f32(60, 1, 1024), datagen.normal_f32(61, 1, 2048)]
+    ws_np, ys, ch = _run_spec(bits, PRODUCED, [3, 3, 1, 2], ext, 0, 700)
+    refs = oracle.gemv_chain(ws_np, [s for _, _, s in PRODUCED], ext, _oracle_fn)
+    first = [y.cpu().numpy() for y in ys]
+    for y, r in zip(first, refs):
+        assert_close(y.astype(np.float64), r)
+    for _ in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        ch.run()
+        torch.cuda.synchronize()
+        assert all(np.array_equal(y.cpu().numpy(), f) for y, f in zip(ys, first))
+    _, ys_p, _ = _run_spec(bits, PRODUCED, [3, 3, 1, 2], ext, qg.QG_FLAG_CHAIN_PERSISTENT, 700)
+    assert all(np.array_equal(y.cpu().numpy(), f) for y, f in zip(ys_p, first))
+    assert qg.device_error() == 0
+
+
 @pytest.mark.parametrize("flags", MODES)
 def test_chain_buffer_reuse_and_repeat(flags):
     """Ping-pong buffers: phase f writes the vector phase f-1 read.  Repeated calls on one

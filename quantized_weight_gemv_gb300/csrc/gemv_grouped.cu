@@ -448,7 +448,8 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
     p.total_qblocks = (int)qblocks;
     p.err = lc.err;
     p.ws = ws;
-    for (int o = 0; o < nout && o < GROUPED_MAX_OUT; ++o) {
+    if (nout < 0 || nout > GROUPED_MAX_OUT || (nout > 0 && !outs)) return QG_ERR_INVALID_ARG;
+    for (int o = 0; o < nout; ++o) {
         const int di = outs[o].desc;
         if (di < 0 || di >= count || internal[di] < 0 || descs[di].n % 32 != 0) return QG_ERR_INVALID_ARG;
         GDesc& d = p.d[internal[di]];

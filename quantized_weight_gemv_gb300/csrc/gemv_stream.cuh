@@ -180,6 +180,11 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     constexpr int R = NB >= SB ? 1 : SB / NB;         // rows per stage
     constexpr int PARTS = NB > SB ? NB / SB : 1;      // stages per row
     constexpr int JU = GEN ? (R * NB + 31) / 32 : JL;  // blocks per lane that can be in a stage
+    // HALF (48-block rows, 10 per 512-block stage): rows 2i and 2i+1 go to the two half
+    // warps, lane l taking blocks 3 (l % 16) .. 3 (l % 16) + 2 of row 2i + l / 16 (j = 3i + q),
+    // so each lane sums its own three blocks per row and a row is reduced over 16 lanes.
+    // Otherwise lane l takes blocks l + 32j of the stage.
+    constexpr bool HALF = GEN && R == 10;
     // distinct activation blocks per lane.  GEN (48 blocks per row): lane l meets blocks
     // (l + 32j) mod 48, and 96 = 0 mod 48, so only the three of j mod 3
     constexpr int NXB = GEN ? 3 : NB >= 32 ? (NB < SB ? NB / 32 : JL) : 1;
@@ -241,7 +246,10 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     if constexpr (XREG) {
 #pragma unroll
         for (int j = 0; j < NXR; ++j) {
-            const int blk = GEN ? (lane + 32 * j) % NB : NB >= 32 ? lane + 32 * j : (lane & (NB - 1));
+            const int blk = HALF  ? 3 * (lane & 15) + j
+                            : GEN ? (lane + 32 * j) % NB
+                            : NB >= 32 ? lane + 32 * j
+                                       : (lane & (NB - 1));
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
                 const XqView v = xq_view(xqbase + c * xstride, NB);
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         unsigned short dh[JU], mh[JU];
 #pragma unroll
         for (int j = 0; j < JU; ++j) {
-            const int fb = lane + 32 * j;
+            const int fb = HALF ? (2 * (j / 3) + (lane >> 4)) * NB + 3 * (lane & 15) + j % 3 : lane + 32 * j;
             if constexpr (BITS == 2) {
                 cw[j] = make_uint4(0u, 0u, 0u, 0u);
                 hw[j] = *reinterpret_cast<const uint2*>(st + 8 * fb);
@@ -315,7 +323,9 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
                     pj[c][j] = combine<BITS>(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), dh[j], mh[j], xs[c][xj],
                                              xS[c][xj]);
                 } else {
-                    const int blk = GEN ? (lane + 32 * j) % NB : (part * SB + lane + 32 * j) & (NB - 1);
+                    const int blk = HALF  ? 3 * (lane & 15) + j % 3
+                                    : GEN ? (lane + 32 * j) % NB
+                                          : (part * SB + lane + 32 * j) & (NB - 1);
                     const XqView v = xq_view(xqbase + c * xstride, NB);
                     const uint4 a = *reinterpret_cast<const uint4*>(v.lo + 16 * blk);
                     const uint4 b = *reinterpret_cast<const uint4*>(v.hi + 16 * blk);
@@ -324,7 +334,29 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
             }
         }
 
-        if constexpr (GEN) {
+        if constexpr (HALF) {
+            // row 2i + l / 16 of lane l: its three blocks j = 3i .. 3i+2; the 5 row pairs
+            // padded to 8 go through one halving tree over each half warp, after which
+            // lane l holds row pair (l % 16) / 2 of its half
+#pragma unroll
+            for (int c = 0; c < BC; ++c) {
+                float rs[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = i < 5 ? 3 * i : 0;  // JU = 15: j + 2 < JU for every row pair
+                    rs[i] = i < 5 ? pj[c][j] + pj[c][j + 1] + pj[c][j + 2] : 0.0f;
+                }
+                halving_reduce<8, 4>(rs);
+                pj[c][0] = rs[0];
+            }
+            const int i = (lane & 15) >> 1, r = 2 * i + (lane >> 4);
+            if ((lane & 1) == 0 && i < 5 && r < rows_u) {
+                float out[BC];
+#pragma unroll
+                for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
+                emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+            }
+        } else if constexpr (GEN) {
             // rows straddle the lanes' block groups: block l + 32j of lane l lies in row
             // (l + 32j) / 48, and every three j cover 96 blocks, two rows - j = 3i is in
             // row 2i, j = 3i+1 in row 2i (lanes 0-15) or 2i+1 (lanes 16-31), j = 3i+2 in

@@ -8,13 +8,18 @@
 //  1. grouped_quantize_kernel: every activation of the group, quantised per block
 //     of 32 (one warp per block) into the caller's workspace;
 //     (A group whose distinct activations are short may skip this launch: the GEMV
-//     kernel then quantises them itself into shared memory, see SMX below.)
+//     kernel then quantises them itself into shared memory, see SMX below.  So may a
+//     group whose images the preceding launch produced: see the images-out tail.)
 //  2. grouped_gemv_kernel (programmatic dependent launch on 1): persistent CTAs
 //     split the concatenated work of all descriptors - units of 256 blocks (whole
 //     rows), or single rows of k/8192 such units for k > 8192 - into contiguous,
 //     equal shares of bulk-copy stages.  Each warp streams its units through a
 //     private ring exactly as the single-matrix streaming kernel does; the ring
 //     starts filling before griddepcontrol.wait, i.e. while kernel 1 still runs.
+//     Optionally (the dependent chain) it also writes the activation images of some
+//     of its outputs for the next launch: the CTA ranges inside those descriptors are
+//     aligned to whole blocks of 32 rows, and each CTA quantises its own rows once
+//     they are stored.
 #include <cstring>
 
 #include "gemv_stream.cuh"

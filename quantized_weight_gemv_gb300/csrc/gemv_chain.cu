@@ -1,12 +1,18 @@
 // Dependent GEMV chain: phases of quantized-weight GEMVs, each phase reading what
-// earlier phases wrote, in one persistent cooperative launch.
+// earlier phases wrote - one grouped launch per phase (default), or one persistent
+// cooperative launch for all of them.
 //
 // A decode token is a chain: every projection quantises and reads a vector that an
 // earlier projection has just written (Gemma WebGPU Engine, "Roadmap": the layer's
 // ordered dispatches, the attention output bound straight into the O projection and
 // its output into the MLP; genie-ai-runtime, "The decode arc": activation quantised
-// per matmul, and "v1.2.0": ~448 dependent kernel launches per token).  One launch
-// per link pays a kernel boundary per link.  Here one CTA per SM walks all phases:
+// per matmul, and "v1.2.0": ~448 dependent kernel launches per token).
+// Per-phase mode: each phase is one grouped launch chained to the one before by
+// programmatic dependent launch; short inputs are quantised by every CTA, and long
+// inputs that are whole outputs of the phase before arrive as activation images that
+// the phase before wrote (its CTA ranges aligned to 32-row blocks), so no phase needs
+// a separate quantisation launch in the decode chain.
+// Persistent mode: one CTA per SM walks all phases:
 //  * A phase is a list of GEMV descriptors whose inputs all exist before it.  Its work
 //    is cut as in the grouped GEMV: units of 256 blocks of 32 (whole rows), or single
 //    rows of k/8192 such units; CTA b takes the units whose first bulk-copy tile lies
@@ -17,7 +23,9 @@
 //    boundary: while the CTA waits for the others at the end of a phase, the ring
 //    fills with the next phase's tiles, up to ~200 KB ahead.
 //  * Fifteen consumer warps take the phase's units round-robin, read each tile's slot
-//    into registers, release it, and compute as the streaming kernels do.
+//    into registers, release it, and compute as the streaming kernels do.  A consumer
+//    waits for a tile's slot only once the producer has published the tile as issued,
+//    which keeps every parity wait within one lap of the ring.
 //  * Between phases (consumers only, named barrier 1): a grid-wide barrier on an
 //    arrival counter in the caller's workspace (fence + atomic add, acquire loads,
 //    bounded by %globaltimer, with an abort word that stops every CTA once one gives

@@ -137,6 +137,7 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
         }
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
+            if (r0 + i * nthreads >= total) break;  // the same for every thread: nothing left in this round
             const int idx_all = r0 + i * nthreads + t;
             const int c = idx_all / nf4;
             const int idx = idx_all - c * nf4;
@@ -179,9 +180,8 @@ __global__ void __launch_bounds__(256) mma_prep_kernel(const float* __restrict__
                                                        unsigned char* __restrict__ img) {
     pdl_wait();
     if (threadIdx.x == 0) pdl_launch_dependents();
-    const int per_cta = 256 * 8;
-    const int item0 = blockIdx.x * per_cta;
-    quantize_to_frags<NT>(X, k, batch, img, threadIdx.x, 256, item0, item0 + per_cta);
+    const int item0 = blockIdx.x * 256;  // one float4 per thread: the image is on the GEMV's critical path
+    quantize_to_frags<NT>(X, k, batch, img, threadIdx.x, 256, item0, item0 + 256);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -396,7 +396,7 @@ static int launch_mma_t(const PlainParams& p, unsigned char* ws, const LaunchCtx
     }
     // 1. the activation image, once; 2. the GEMV, chained by programmatic dependent launch
     const int items = 8 * NT * (p.k >> 2);
-    const int pgrid = (items + 256 * 8 - 1) / (256 * 8);
+    const int pgrid = (items + 255) / 256;
     int rc = launch_kernel(mma::mma_prep_kernel<NT>, dim3(pgrid), dim3(256), 0, lc, p.x, p.k, p.batch, ws);
     if (rc != QG_OK) return rc;
     auto kern = mma::mma_batched_kernel<NT, true>;

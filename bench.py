@@ -511,11 +511,23 @@ def cpu_baseline(budget_s):
                 break
         sample.append(layer)
         layer += 1
+    # and the single 1024 x 1024 Q4 GEMV on one host thread (best of 5 calls)
+    import oracle
+
+    w1, x1 = W.q4_single()
+    t1 = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        oracle.gemv(w1, x1)
+        t1.append(time.perf_counter() - t0)
+    one = min(t1)
     return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{done_gemv} full GEMVs of decode layers {sample[0]}..{sample[-1]} "
                       f"({done_bytes / 1e6:.0f} MB of packed weights, fp64 scalar C, rows split over "
                       f"{cores} host threads)",
-            "seconds": t_total, "gemv_per_s": done_gemv / t_total}
+            "seconds": t_total, "gemv_per_s": done_gemv / t_total,
+            "single_core_q4_1024x1024": {"ms_per_gemv": one * 1e3,
+                                         "GBps": W.q4_bytes(1024, 1024) / one / 1e9, "cores": 1}}
 
 
 # ------------------------------------------------------------------ arms

@@ -142,12 +142,7 @@ def run_case(args):
     if bits in (2, 6):
         ws = qg.vocab_workspace(device)
         am = torch.empty(1, dtype=torch.int32, device=device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for i in range(args.reps * copies):
-        r = rot[i % copies]
+    def call(r):
         if batch > 1:
             qg.qgemv_batched(4, r["lo"], None, r["scale"], r["min"], x, Y=y)
         elif bits == 4:
@@ -155,6 +150,15 @@ def run_case(args):
         else:
             qg.vocab_softcap_argmax(bits, r["lo"], r.get("hi"), r["scale"], r.get("min"), x[0], W.SOFTCAP,
                                     logits=y[0], argmax=am, ws=ws)
+
+    for r in rot[:2]:  # untimed: one-time kernel attributes and module loading
+        call(r)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(args.reps * copies):
+        call(rot[i % copies])
     e1.record()
     torch.cuda.synchronize()
     calls = args.reps * copies

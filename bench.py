@@ -582,6 +582,23 @@ def run_reference(args, ws, rank):
     print(json.dumps(out), flush=True)
 
 
+def ranks_max(pg, value, device=None):
+    """The largest `value` over all ranks (the slowest rank's timed region sets the step);
+    `value` itself without a process group."""
+    if pg is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(world, bytes_per_rank, ms_step):
+    """Whole-job GB/s: the packed bytes every rank streams in one step, over the step time."""
+    return world * bytes_per_rank / (ms_step * 1e-3) / 1e9
+
+
 def run_ours(args, ws, rank, local):
     import torch
 
@@ -652,13 +669,9 @@ def run_ours(args, ws, rank, local):
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    ms_total = e0.elapsed_time(e1)
-    if pg:
-        tt = torch.tensor([ms_total], device=device)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = ranks_max(pg, e0.elapsed_time(e1), device)
     ms_step = ms_total / args.steps
-    value = ws * total_bytes / (ms_step * 1e-3) / 1e9  # GB/s, all ranks
+    value = job_gbps(ws, total_bytes, ms_step)  # GB/s, all ranks
     med, p95 = time_graph_stats(g, stream, 50, warm=2, repeats=20)
     step_stats = {"median_ms": med, "p95_ms": p95, "repeats": 20, "replays_per_repeat": 50,
                   "median_GBps": total_bytes / (med * 1e-3) / 1e9}

@@ -501,7 +501,8 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
     // caller's flags).  Default: two CTAs per SM (16 warps, at most 128 registers each)
     // and one ring slot per warp - measured on GB300 as the fastest shape: the slot is
     // refilled as soon as it has been copied to registers, so 16 x 5 KB stay in flight
-    // per SM.  The diagnostic switches QG_GROUPED_CTAS_PER_SM (1 or 2) and
+    // per SM.  The diagnostic switches QG_GROUPED_CTAS_PER_SM (1 or 2: the kernel's
+    // register bound), QG_GROUPED_GRID_PER_SM (1 or 2: the grid, by default the same) and
     // QG_GROUPED_SLOTS (slots per warp) override it.
     int per_sm = env_int("QG_GROUPED_CTAS_PER_SM", 2);
     if (per_sm < 1) per_sm = 1;

@@ -27,7 +27,8 @@
 //  * the activation image is made once per call into a workspace (prep kernel) and
 //    pulled into shared memory with one bulk copy; 16 warps per CTA share it.
 //  * a warp's task is one half of the k range of one group of 16 rows: 1-4 tiles of
-//    16 rows x 8 blocks, all put in flight at once through a private cp.async ring
+//    16 rows x 8 blocks, put in flight at once through a private cp.async ring (all of
+//    them for 8 columns, 3 at a time for 9-16)
 //    (rows padded to 144 bytes so that the fragment reads are bank-conflict free);
 //    warps w and w^1 take the two halves of a row group and add their partial sums
 //    through shared memory under a named barrier of the pair (half 0 + half 1, in

@@ -477,6 +477,34 @@ def test_vocab_softcap_select(bits):
             assert abs(float(lp.item()) - ref_lp) <= TOL * max(1.0, abs(ref_lp))
 
 
+@pytest.mark.parametrize("bits", [2, 4, 6])
+@pytest.mark.parametrize("n", [1, 7, 33, 300, 1025])
+def test_vocab_softcap_select_small_vocab(bits, n):
+    """The one-launch selection on vocabularies smaller than or not divisible by the grid:
+    every CTA's row range holds a few rows or one; no list, only out-of-range ids, one
+    allowed id, and a duplicated list."""
+    k = 1536 if bits == 2 else 2048
+    w = datagen.make_quantized(bits, 1300 + n, n, k)
+    x = datagen.normal_f32(1300 + n, 1, k)
+    wd = dev_w(w)
+    xt = torch.from_numpy(x).to(DEV)
+    ws = qg.vocab_select_workspace(DEV)
+    lists = (None, np.array([-1, n, n + 3], np.int32), np.array([n - 1], np.int32),
+             np.array([0, n // 2, 0, n // 2, n - 1], np.int32))
+    for allowed in lists:
+        at = None if allowed is None else torch.from_numpy(allowed).to(DEV)
+        logits, tok, lp = qg.vocab_softcap_select(bits, wd["lo"], wd.get("hi"), wd["scale"], wd["min"], xt, 30.0,
+                                                  allowed=at, ws=ws)
+        l = logits.cpu().numpy()
+        own_tok, own_lp = oracle.select(l.astype(np.float64), allowed)
+        assert int(tok.item()) == own_tok, (allowed, int(tok.item()), own_tok)
+        if own_tok < 0:
+            assert np.isnan(float(lp.item()))
+        else:
+            assert abs(float(lp.item()) - own_lp) <= TOL * max(1.0, abs(own_lp))
+    # the four calls share one workspace: a counter left armed would break the next merge
+
+
 # ---------------------------------------------------------------- 2-bit codes, zero point 2
 def test_q2_zero_point_closed_forms():
     """Codes 2 decode to zero weights (y = 0 exactly); codes 3 give y = scale * sum(x_deq)."""

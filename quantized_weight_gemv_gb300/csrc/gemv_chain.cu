@@ -367,7 +367,8 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CP
         }
     } else {
         // ---------------- consumers
-        int base = 0;  // tiles of this CTA in earlier phases
+        int base = 0;     // tiles of this CTA in earlier phases
+        int issued = 0;   // tiles this lane has seen published as issued
         for (int f = 0; f < p.nphase; ++f) {
             // Phase boundary.  The consumers take each consumer_sync the same number of
             // times: s_abort changes only between the first two (thread 0) or after the
@@ -399,9 +400,15 @@ __global__ void __launch_bounds__(NT, 1) chain_kernel(const __grid_constant__ CP
                 for (int part = 0; part < parts; ++part) {
                     const int n = base + tile_index(d, u, part) - r.t0;
                     const int slot = n & (NS - 1);
-                    // all lanes poll; the decision is taken together so that the warp stays converged
-                    const bool ready = wait_issued(&s_issued, n, &s_abort);
-                    __threadfence_block();
+                    // all lanes poll; the decision is taken together so that the warp stays converged.
+                    // The published count is re-read only once this tile lies beyond the last
+                    // one seen (the producer normally runs ahead).
+                    bool ready = true;
+                    if (n >= issued) {
+                        ready = wait_issued(&s_issued, n, &s_abort);
+                        issued = s_issued;
+                        __threadfence_block();
+                    }
                     if (!__all_sync(0xffffffffu, ready && stream::mbar_wait(&full[slot], (uint32_t)((n >> LS) & 1)))) {
                         if (lane == 0) atomicOr(p.err, ERR_WAIT_FULL);
                         s_abort = 1;

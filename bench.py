@@ -27,6 +27,9 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 METRIC = "effective weight GB/s & GEMV/s at batch 1 (fraction of ~8 TB/s HBM)"
+# end-to-end leg: untimed warm-up steps (at least) and timed steps, independent of --steps
+E2E_WARMUP = 10
+E2E_STEPS = 100
 
 # DRAM bytes (read + write) per launch of the timed kernel, from one ncu capture of the
 # full decode-layer stream (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None
@@ -51,12 +54,16 @@ def parse():
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one kernel workload a few times and exit (a small case for profilers)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--graph", action="store_true",
+                    help="--case: time one round over the copies captured in a CUDA graph with PDL")
     return ap.parse_args()
 
 
 # name -> (bits, n, k, rotation copies); copies make the working set exceed L2
 CASES = {
+    "q4_single_1024x1024": (4, 1024, 1024, 512),
     "q4_gate_16384x2048": (4, 16384, 2048, 8),
+    "q4_batched_b2_16384x2048": (4, 16384, 2048, 8),
     "q4_down_2048x16384": (4, 2048, 16384, 8),
     "q4_q_2048x2048": (4, 2048, 2048, 64),
     "q6_vocab_262144x2048": (6, 262144, 2048, 1),
@@ -64,6 +71,8 @@ CASES = {
     "q4_batched_b4_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b8_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
+    "cq_8192x512": None,  # the CQ matvec, 64 rotating copies (run_cq_case)
+    "select_262144": None,  # constrained selection over 262144 logits, 1 % allowed (run_select_case)
     "q4_chain_persistent": None,  # the decode chain, --layers layers (run_chain_case)
     "q4_chain_launches": None,
     "q4_decode_stream": None,  # the --layers-layer decode stream as one grouped call (run_stream_case)
@@ -119,6 +128,52 @@ def run_stream_case(args):
           flush=True)
 
 
+def run_cq_case(args):
+    """Profiling case: the 8192 x 512 CQ matvec over 64 rotating copies (> L2), --reps rounds."""
+    import torch
+
+    import quantized_weight_gemv_gb300 as qg
+    from datagen import workloads as W
+
+    device = torch.device("cuda", 0)
+    m = qg.to_device(W.cq_matrix(0), device)
+    rot = [m] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in m.items()} for _ in range(63)]
+    xc = torch.from_numpy(W.cq_x()).to(device)
+    yc = torch.empty(W.CQ_ROWS[0], device=device)
+    state = {"i": 0}
+
+    def call():
+        r = rot[state["i"] % 64]
+        state["i"] += 1
+        qg.cq_fwht_matvec(r["idx"], r["codebook"], r["row_scale"], xc, W.CQ_GROUP, y=yc, flags=qg.QG_FLAG_PDL)
+
+    ms = time_eager(call, torch.cuda.current_stream(device), args.reps * 64)
+    nbytes = W.cq_bytes(W.CQ_ROWS[0], W.CQ_K)
+    print(json.dumps({"case": args.case, "calls": args.reps * 64, "us_per_call_eager": ms * 1e3,
+                      "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
+
+
+def run_select_case(args):
+    """Profiling case: constrained selection over 262144 seeded logits with the benchmark's
+    allowed list (about 1 % of the ids), --reps calls."""
+    import torch
+
+    import datagen
+    import quantized_weight_gemv_gb300 as qg
+    from datagen import workloads as W
+
+    device = torch.device("cuda", 0)
+    logits = torch.from_numpy(datagen.normal_f32(12, 1, W.VOCAB) * np.float32(5.0)).to(device)
+    allowed = torch.from_numpy(W.select_allowed()).to(device)
+    tok = torch.empty(1, dtype=torch.int32, device=device)
+    lp = torch.empty(1, dtype=torch.float32, device=device)
+    ws = qg.select_workspace(device)
+    ms = time_eager(lambda: qg.qg_logits_select(logits, allowed, token=tok, logprob=lp, ws=ws),
+                    torch.cuda.current_stream(device), args.reps)
+    print(json.dumps({"case": args.case, "calls": args.reps, "us_per_call_eager": ms * 1e3,
+                      "logits": W.VOCAB, "allowed": int(allowed.numel())}), flush=True)
+
+
 def run_case(args):
     """A small profiling case: seeded weights of one shape, rotated over copies (> L2), called reps times."""
     import torch
@@ -126,6 +181,10 @@ def run_case(args):
         return run_chain_case(args)
     if args.case == "q4_decode_stream":
         return run_stream_case(args)
+    if args.case == "cq_8192x512":
+        return run_cq_case(args)
+    if args.case == "select_262144":
+        return run_select_case(args)
 
     import quantized_weight_gemv_gb300 as qg
     from datagen import workloads as W
@@ -142,27 +201,36 @@ def run_case(args):
     if bits in (2, 6):
         ws = qg.vocab_workspace(device)
         am = torch.empty(1, dtype=torch.int32, device=device)
+    fl = qg.QG_FLAG_PDL if args.graph else 0
+
     def call(r):
         if batch > 1:
-            qg.qgemv_batched(4, r["lo"], None, r["scale"], r["min"], x, Y=y)
+            qg.qgemv_batched(4, r["lo"], None, r["scale"], r["min"], x, Y=y, flags=fl)
         elif bits == 4:
-            qg.qgemv_q4(r["lo"], r["scale"], r["min"], x[0], y=y[0])
+            qg.qgemv_q4(r["lo"], r["scale"], r["min"], x[0], y=y[0], flags=fl)
         else:
             qg.vocab_softcap_argmax(bits, r["lo"], r.get("hi"), r["scale"], r.get("min"), x[0], W.SOFTCAP,
-                                    logits=y[0], argmax=am, ws=ws)
+                                    logits=y[0], argmax=am, ws=ws, flags=fl)
 
+    calls = args.reps * copies
+    nbytes = {2: W.q2_bytes, 4: W.q4_bytes, 6: W.q6_bytes}[bits](n, k)
+    if args.graph:  # one round over the copies captured in a graph (PDL), replayed --reps times
+        st = torch.cuda.Stream(device)
+        g = graph_of(lambda: [call(r) for r in rot], st)
+        ms = time_graph(g, st, args.reps, repeats=5) / copies
+        print(json.dumps({"case": args.case, "batch": batch, "calls": calls, "us_per_call_graph": ms * 1e3,
+                          "GBps_graph": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
+        return
     for r in rot[:2]:  # untimed: one-time kernel attributes and module loading
         call(r)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record()
-    for i in range(args.reps * copies):
+    for i in range(calls):
         call(rot[i % copies])
     e1.record()
     torch.cuda.synchronize()
-    calls = args.reps * copies
-    nbytes = {2: W.q2_bytes, 4: W.q4_bytes, 6: W.q6_bytes}[bits](n, k)
     ms = e0.elapsed_time(e1) / calls
     print(json.dumps({"case": args.case, "batch": batch, "calls": calls, "us_per_call_eager": ms * 1e3,
                       "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
@@ -454,6 +522,33 @@ def extra_rows(device):
     del rot, wbd
     torch.cuda.empty_cache()
 
+    # the plain-read floor: one kernel that only reads a buffer of the same 20,971,520 bytes
+    # once, in the same setting (24 rotating buffers, programmatic dependent launch, graph)
+    bufs = [torch.empty(nbytes, dtype=torch.uint8, device=device).fill_(i) for i in range(copies)]
+    acc = torch.zeros(1, dtype=torch.int32, device=device)
+    g = graph_of(lambda: [qg.qg_read_floor(b, out=acc, flags=qg.QG_FLAG_PDL) for b in bufs], st)
+    ms = time_graph(g, st, 10) / copies
+    rows["read_floor_20971520B"] = {"us_per_call": ms * 1e3, "GBps": nbytes / ms / 1e6,
+                                    "what": "qg_read_floor over 24 rotating 21 MB buffers (graph, PDL): the time "
+                                            "of a kernel that only reads the bytes of one 16384x2048 Q4 matrix"}
+    del bufs, g
+    torch.cuda.empty_cache()
+
+    # the down projection (2048 x 16384, short N / long K) as one call per matrix
+    wdn = qg.to_device(W.decode_projection(0, 6)[0], device)
+    xdn = torch.from_numpy(W.decode_projection(0, 6)[1]).to(device)
+    ydn = torch.empty(2048, device=device)
+    rot = [wdn] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in wdn.items()}
+                   for _ in range(copies - 1)]
+    g = graph_of(lambda: [qg.qgemv_q4(r["lo"], r["scale"], r["min"], xdn, y=ydn, flags=qg.QG_FLAG_PDL)
+                          for r in rot], st)
+    ms = time_graph(g, st, 10) / copies
+    nb_dn = W.q4_bytes(2048, W.FFN)
+    rows["q4_down_2048x16384"] = {"us_per_call": ms * 1e3, "GBps": nb_dn / ms / 1e6,
+                                  "what": "one qgemv_q4 call per matrix, 24 rotating copies (graph, PDL)"}
+    del rot, wdn, g
+    torch.cuda.empty_cache()
+
     # CQ matvec, K = 512, 8192 and 1024 rows
     xc = torch.from_numpy(W.cq_x()).to(device)
     for which, n in enumerate(W.CQ_ROWS):
@@ -572,14 +667,25 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode_layers (35 layers x 7 Q4 projections, hidden 2048, FFN 16384); "
-                               f"per step a {rows_per_step}-row slice of one layer-0 projection, cycling",
-                   "oracle": f"fp64 scalar C, rows split over {cores} host threads"},
+        "config": workload_config(args.layers, args.gpus),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"per step: {rows_per_step} rows of one of the 7 layer-0 projections, cycling"},
+                         "sample": f"per step: {rows_per_step} rows of one of the 7 layer-0 projections of the "
+                                   f"decode stream, cycling (fp64 scalar C, rows split over {cores} host threads)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
+
+
+def workload_config(n_layers, world):
+    """The `config` object of the JSON line, the same for both arms."""
+    from datagen import workloads as W
+
+    n_gemv = 7 * n_layers
+    total = W.decode_pass_bytes(n_layers)
+    return {"workload": f"decode_layers: {n_layers} layers x 7 Q4 projections (hidden 2048, FFN 16384), "
+                        f"{n_gemv} GEMVs, {total / 1e9:.3f} GB packed weights, batch 1",
+            "l2": "inputs larger than L2 (no flush needed)",
+            "parallelism": f"replicas x{world}"}
 
 
 def ranks_max(pg, value, device=None):
@@ -680,17 +786,40 @@ def run_ours(args, ws, rank, local):
     # activations from pinned host memory, runs the 245 calls (replayed graph of the
     # captured calls) and copies all outputs back.  Serial: one step after the other on
     # one stream.  Pipelined (reported): two device/host buffer sets, the H2D of step
-    # i+1 and the D2H of step i on copy streams under the compute of step i.
-    e2e_steps = max(5, min(args.steps, 100))
+    # i+1 and the D2H of step i on copy streams under the compute of step i.  Both loops
+    # run E2E_WARMUP untimed steps first and then a fixed E2E_STEPS timed steps, whatever
+    # --steps is, so that one-time costs (first copies from a pinned buffer, first use of
+    # a stream) stay out of the figure.
+    e2e_warm = max(E2E_WARMUP, args.warmup)
+    ev_parts = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(E2E_STEPS)]
+
+    def serial_step(evs=None):
+        with torch.cuda.stream(stream):
+            if evs:
+                evs[0].record(stream)
+            x_dev.copy_(x_host, non_blocking=True)
+            if evs:
+                evs[1].record(stream)
+            g.replay()
+            if evs:
+                evs[2].record(stream)
+            y_host.copy_(y_dev, non_blocking=True)
+            if evs:
+                evs[3].record(stream)
+        stream.synchronize()
+
+    for _ in range(e2e_warm):
+        serial_step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        with torch.cuda.stream(stream):
-            x_dev.copy_(x_host, non_blocking=True)
-            g.replay()
-            y_host.copy_(y_dev, non_blocking=True)
-        stream.synchronize()
-    serial_s = (time.perf_counter() - t0) / e2e_steps
+    for i in range(E2E_STEPS):
+        serial_step(ev_parts[i])
+    serial_s = (time.perf_counter() - t0) / E2E_STEPS
+    parts = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                      for e in ev_parts])
+    serial_breakdown = {"h2d_ms": float(np.median(parts[:, 0])), "compute_ms": float(np.median(parts[:, 1])),
+                        "d2h_ms": float(np.median(parts[:, 2])),
+                        "host_gap_ms": serial_s * 1e3 - float(np.median(parts.sum(axis=1)))}
 
     x_dev2 = torch.empty_like(x_dev)
     y_dev2 = torch.empty_like(y_dev)
@@ -708,35 +837,42 @@ def run_ours(args, ws, rank, local):
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_read = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined(steps):
+        for i in range(steps):
+            b = i & 1
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(ev_done[b])  # step i-2 has finished reading this x buffer
+                xds[b].copy_(x_host, non_blocking=True)
+                ev_in[b].record(h2d)
+            with torch.cuda.stream(stream):
+                stream.wait_event(ev_in[b])
+                if i >= 2:
+                    stream.wait_event(ev_read[b])  # step i-2's outputs are on the host
+                graphs[b].replay()
+                ev_done[b].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev_done[b])
+                yhs[b].copy_(yds[b], non_blocking=True)
+                ev_read[b].record(d2h)
+
+    pipelined(e2e_warm)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        b = i & 1
-        with torch.cuda.stream(h2d):
-            if i >= 2:
-                h2d.wait_event(ev_done[b])  # step i-2 has finished reading this x buffer
-            xds[b].copy_(x_host, non_blocking=True)
-            ev_in[b].record(h2d)
-        with torch.cuda.stream(stream):
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_read[b])  # step i-2's outputs are on the host
-            graphs[b].replay()
-            ev_done[b].record(stream)
-        with torch.cuda.stream(d2h):
-            d2h.wait_event(ev_done[b])
-            yhs[b].copy_(yds[b], non_blocking=True)
-            ev_read[b].record(d2h)
+    pipelined(E2E_STEPS)
     torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = (time.perf_counter() - t0) / E2E_STEPS
     # the last step's outputs reached the host intact
-    if not torch.equal(yhs[(e2e_steps - 1) & 1], yds[(e2e_steps - 1) & 1].cpu()):
+    if not torch.equal(yhs[(E2E_STEPS - 1) & 1], yds[(E2E_STEPS - 1) & 1].cpu()):
         raise RuntimeError("pipelined end-to-end outputs differ from the device outputs")
     e2e = {"value": ws * total_bytes / e2e_s / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4),
-           "ms_per_step": e2e_s * 1e3, "serial_ms_per_step": serial_s * 1e3,
+           "ms_per_step": e2e_s * 1e3, "serial_ms_per_step": serial_s * 1e3, "steps": E2E_STEPS,
+           "warmup": e2e_warm, "serial_breakdown": serial_breakdown,
            "pipelining": "two buffer sets; H2D of step i+1 and D2H of step i on copy streams under the "
-                         "compute of step i (serial_ms_per_step: one step after the other)"}
+                         "compute of step i (serial_ms_per_step: one step after the other; serial_breakdown: "
+                         "median CUDA-event times of its parts and the host time around them)"}
     del g2, graphs
 
     # ---- the other launch mode, for comparison (same graph timing, fewer steps)
@@ -783,16 +919,13 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": f"decode_layers: {n_layers} layers x 7 Q4 projections (hidden 2048, FFN 16384), "
-                               f"{n_gemv} GEMVs, {total_bytes / 1e9:.3f} GB packed weights, batch 1",
-                   "launch": ("one qgemv_grouped call per step over the 245 descriptors (activation quantisation "
-                              "+ grouped GEMV, chained by programmatic dependent launch), captured in a CUDA graph"
-                              if args.launch == "grouped" else
-                              "one qgemv_q4 call per GEMV, programmatic dependent launch, captured in a CUDA graph"),
-                   "l2": "inputs larger than L2 (no flush needed)",
-                   "gemv_per_s": ws * n_gemv / (ms_step * 1e-3),
-                   "frac_of_8TBps": value / ws / 8000.0,
-                   "parallelism": f"replicas x{ws}"},
+        "config": workload_config(n_layers, ws),
+        "launch": ("one qgemv_grouped call per step over the 245 descriptors (activation quantisation "
+                   "+ grouped GEMV, chained by programmatic dependent launch), captured in a CUDA graph"
+                   if args.launch == "grouped" else
+                   "one qgemv_q4 call per GEMV, programmatic dependent launch, captured in a CUDA graph"),
+        "gemv_per_s": ws * n_gemv / (ms_step * 1e-3),
+        "frac_of_8TBps": value / ws / 8000.0,
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

@@ -313,6 +313,18 @@ int qg_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int
 int qg_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,
                  void* stream);
 
+/*
+ * qg_read_floor: a measurement hook, not part of the method.  Reads every byte of
+ * src[0, bytes) once (16-byte streaming loads) and XORs the 32-bit words into *out.
+ * The time of this call is the floor of any kernel that streams the same bytes in the
+ * same launch setting, which is what the GEMVs' weight streams are compared with
+ * (the decode bound of the oxinfer README, "Performance": every weight byte is read
+ * once per token).  The reads may start before the preceding work finishes under
+ * QG_FLAG_PDL; *out is updated after it.
+ *   src : device, 16-byte aligned;  bytes > 0, bytes % 16 == 0;  out : device uint32 [1]
+ */
+int qg_read_floor(const void* src, size_t bytes, uint32_t* out, unsigned flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

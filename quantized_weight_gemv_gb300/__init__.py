@@ -56,6 +56,7 @@ SIGNATURES = {
     "qgemv_chain": (_i, [_i, _vp, _i, _vp, _i, _vp, _sz, _u, _vp]),
     "qg_quantize_act": (_i, [_f32p, _i, _i, _i8p, _f32p, _i32p, _vp]),
     "qg_blockdots": (_i, [_i, _u8p, _u8p, _i, _i, _i8p, _i32p, _vp]),
+    "qg_read_floor": (_i, [_vp, _sz, _vp, _u, _vp]),
 }
 
 _lock = threading.Lock()
@@ -436,6 +437,21 @@ def qg_blockdots(bits, lo, hi, xq):
         _check(lib().qg_blockdots(bits, _ptr(lo), _ptr(hi) if bits == 6 else None, n, k, _ptr(xq), _ptr(dots),
                                   _stream(dev)), "qg_blockdots")
     return dots
+
+
+def qg_read_floor(buf, out=None, flags: int = 0):
+    """Read every byte of the device tensor `buf` once (the plain-read floor); returns the
+    uint32 XOR of its words in `out` (an int32 [1] device tensor, XOR-accumulated)."""
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    dev = buf.device
+    if out is None:
+        out = torch.zeros(1, dtype=torch.int32, device=dev)
+    _need(out, "out", (torch.int32,), dev)
+    with torch.cuda.device(dev):
+        _check(lib().qg_read_floor(_ptr(buf), buf.numel() * buf.element_size(), _ptr(out), flags, _stream(dev)),
+               "qg_read_floor")
+    return out
 
 
 def device_error() -> int:

@@ -125,6 +125,29 @@ static int gemv_common(int bits, const uint8_t* lo, const uint8_t* hi, const uin
     return launch_plain(pp, bits, EPI_STORE, lc);
 }
 
+// The descriptor list of a grouped call: bits 4 or 6, 0 <= count <= QG_MAX_GROUP, every
+// descriptor with n >= 0 and k a power of two in [1024, 16384], and the weights, x and y
+// of every non-empty one present and aligned.  *active receives the non-empty count.
+int check_grouped(int bits, const qg_gemv_desc* descs, int count, int* active) {
+    *active = 0;
+    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
+    if (count < 0 || count > QG_MAX_GROUP) return QG_ERR_INVALID_ARG;
+    if (count == 0) return QG_OK;
+    if (!descs) return QG_ERR_INVALID_ARG;
+    for (int i = 0; i < count; ++i) {
+        const qg_gemv_desc& d = descs[i];
+        if (d.n < 0) return QG_ERR_INVALID_ARG;
+        if (d.k < 1024 || d.k > 16384 || (d.k & (d.k - 1)) != 0) return QG_ERR_UNSUPPORTED;
+        if (d.n == 0) continue;
+        int rc = check_weights(bits, d.lo, d.hi, d.scale, d.min, d.n, d.k);
+        if (rc != QG_OK) return rc;
+        if (!d.x || !d.y) return QG_ERR_INVALID_ARG;
+        if (!aligned16(d.x) || !aligned16(d.y)) return QG_ERR_ALIGNMENT;
+        ++*active;
+    }
+    return QG_OK;
+}
+
 }  // namespace qg
 
 using namespace qg;
@@ -374,27 +397,13 @@ int qgemv_chain(int bits, const qg_gemv_desc* descs, int count, const int* phase
 
 int qgemv_grouped(int bits, const qg_gemv_desc* descs, int count, void* ws, size_t ws_bytes, unsigned flags,
                   void* stream) {
-    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
-    if (count < 0 || count > QG_MAX_GROUP) return QG_ERR_INVALID_ARG;
-    if (count == 0) return QG_OK;
-    if (!descs) return QG_ERR_INVALID_ARG;
     int active = 0;
-    for (int i = 0; i < count; ++i) {
-        const qg_gemv_desc& d = descs[i];
-        if (d.n < 0) return QG_ERR_INVALID_ARG;
-        if (d.k < 1024 || d.k > 16384 || (d.k & (d.k - 1)) != 0) return QG_ERR_UNSUPPORTED;
-        if (d.n == 0) continue;
-        int rc = check_weights(bits, d.lo, d.hi, d.scale, d.min, d.n, d.k);
-        if (rc != QG_OK) return rc;
-        if (!d.x || !d.y) return QG_ERR_INVALID_ARG;
-        if (!aligned16(d.x) || !aligned16(d.y)) return QG_ERR_ALIGNMENT;
-        ++active;
-    }
-    if (active == 0) return QG_OK;
+    int rc = check_grouped(bits, descs, count, &active);
+    if (rc != QG_OK || active == 0) return rc;
     if (!ws || ws_bytes < grouped_workspace_bytes(descs, count)) return QG_ERR_WORKSPACE;
     if (!aligned16(ws)) return QG_ERR_ALIGNMENT;
     LaunchCtx lc;
-    int rc = resolve(stream, flags, lc);
+    rc = resolve(stream, flags, lc);
     if (rc != QG_OK) return rc;
     return launch_grouped(bits, descs, count, reinterpret_cast<unsigned char*>(ws), lc);
 }
@@ -407,6 +416,15 @@ int qg_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int
     int rc = resolve(stream, 0, lc);
     if (rc != QG_OK) return rc;
     return launch_quantize_act(x, k, batch, xq, xs, xsum, lc);
+}
+
+int qg_read_floor(const void* src, size_t bytes, uint32_t* out, unsigned flags, void* stream) {
+    if (!src || !out || bytes == 0 || (bytes & 15) != 0) return QG_ERR_INVALID_ARG;
+    if (!aligned16(src)) return QG_ERR_ALIGNMENT;
+    LaunchCtx lc;
+    int rc = resolve(stream, flags, lc);
+    if (rc != QG_OK) return rc;
+    return launch_read_floor(src, bytes, out, lc);
 }
 
 int qg_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,

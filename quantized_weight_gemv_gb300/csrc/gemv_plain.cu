@@ -166,6 +166,42 @@ int launch_plain(const PlainParams& p, int bits, int epi, const LaunchCtx& lc) {
     return QG_ERR_UNSUPPORTED;
 }
 
+// The plain-read floor: every 16-byte word of src read once with streaming loads (four
+// per thread in flight), XOR-folded into *out.  The time of a kernel that only reads a
+// buffer once is the floor of any kernel streaming the same bytes in the same launch
+// setting (the decode bound of the oxinfer README, "Performance": every weight byte is
+// read once per token).  The reads start before griddepcontrol.wait, as the GEMV
+// kernels' weight streams do; *out is written after it.
+__global__ void __launch_bounds__(512) read_floor_kernel(const uint4* __restrict__ src, size_t n16, uint32_t* out) {
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t acc = 0;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = ldg_stream16(src + i), b = ldg_stream16(src + i + stride);
+        const uint4 c = ldg_stream16(src + i + 2 * stride), d = ldg_stream16(src + i + 3 * stride);
+        acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+    }
+    for (; i < n16; i += stride) {
+        const uint4 a = ldg_stream16(src + i);
+        acc ^= a.x ^ a.y ^ a.z ^ a.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+    pdl_wait();
+    if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
+}
+
+int launch_read_floor(const void* src, size_t bytes, uint32_t* out, const LaunchCtx& lc) {
+    const size_t n16 = bytes >> 4;
+    long long grid = (long long)lc.sm_count * 4;  // 2048 threads per SM
+    const long long need = (long long)((n16 + 511) / 512);
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    return launch_kernel(read_floor_kernel, dim3((unsigned)grid), dim3(512), 0, lc,
+                         reinterpret_cast<const uint4*>(src), n16, out);
+}
+
 int launch_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, const LaunchCtx& lc) {
     const long long blocks = (long long)batch * (k >> 5);
     long long grid = (blocks + 7) / 8;

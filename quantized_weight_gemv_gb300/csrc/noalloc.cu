@@ -54,15 +54,15 @@ int scratch_address(void** out) {
 }  // namespace
 
 extern "C" int qgemv_grouped_noalloc(int bits, const qg_gemv_desc* descs, int count, unsigned flags, void* stream) {
-    if (bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;
-    if (count < 0 || count > QG_MAX_GROUP) return QG_ERR_INVALID_ARG;
-    if (count == 0) return QG_OK;
-    if (!descs) return QG_ERR_INVALID_ARG;
-    // the group's quantised activations must fit the fixed scratch
+    // the descriptors first, exactly as qgemv_grouped checks them (so a bad k or n gives
+    // the same status as there), then the size of the group's quantised activations
+    int active = 0;
+    int rc = qg::check_grouped(bits, descs, count, &active);
+    if (rc != QG_OK || active == 0) return rc;
     if (qg_grouped_workspace_bytes(descs, count) > (size_t)QG_NOALLOC_WS_BYTES) return QG_ERR_WORKSPACE;
     void* ws = nullptr;
-    const int rc = scratch_address(&ws);
+    rc = scratch_address(&ws);
     if (rc != QG_OK) return rc;
-    // everything else is validated, and the work launched, by the allocating entry point
+    // the work is launched by the allocating entry point, on the fixed scratch
     return qgemv_grouped(bits, descs, count, ws, (size_t)QG_NOALLOC_WS_BYTES, flags, stream);
 }

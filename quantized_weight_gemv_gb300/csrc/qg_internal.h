@@ -104,6 +104,8 @@ size_t mma_workspace_bytes(int k, int batch);
 // ws: the activation image (mma_workspace_bytes), or null to quantise in every CTA
 int launch_mma(const PlainParams& p, unsigned char* ws, const LaunchCtx& lc);
 size_t grouped_workspace_bytes(const qg_gemv_desc* descs, int count);
+// descriptor checks shared by qgemv_grouped and qgemv_grouped_noalloc (capi.cu)
+int check_grouped(int bits, const qg_gemv_desc* descs, int count, int* active);
 // Whether launch_grouped(..., fuse = true) takes the one-launch form for this group:
 // its distinct activations (by x and k) are short enough to be quantised in every CTA.
 bool grouped_fuses(const qg_gemv_desc* descs, int count);
@@ -127,6 +129,7 @@ int launch_chain(int bits, const qg_gemv_desc* descs, int count, const int* phas
                  unsigned char* ws, const LaunchCtx& lc);
 int launch_select(const float* logits, int n, const int32_t* allowed, int n_allowed, int32_t* token, float* logprob,
                   SelectWorkspace* ws, const LaunchCtx& lc);
+int launch_read_floor(const void* src, size_t bytes, uint32_t* out, const LaunchCtx& lc);
 int launch_quantize_act(const float* x, int k, int batch, int8_t* xq, float* xs, int32_t* xsum, const LaunchCtx& lc);
 int launch_blockdots(int bits, const uint8_t* lo, const uint8_t* hi, int n, int k, const int8_t* xq, int32_t* dots,
                      const LaunchCtx& lc);

@@ -143,11 +143,11 @@ def decode_chain():
     mats = [dev_w(w) for w in ws_np]
     x0 = W.decode_chain_x()
     refs = oracle.gemv_chain(ws_np, src, [x0], _oracle_fn)
-    return src, stages, mats, x0, refs
+    return src, stages, mats, x0, refs, ws_np
 
 
 def _decode_run(dc, flags, x0=None):
-    src, stages, mats, x_ref, _ = dc
+    src, stages, mats, x_ref, _, _ = dc
     X = torch.from_numpy(x_ref if x0 is None else x0).to(DEV)
     ys = [torch.full((W.PROJ_SHAPES[j % 7][0],), float("nan"), device=DEV) for j in range(len(src))]
     xs = [X if s < 0 else ys[s] for s in src]
@@ -164,23 +164,29 @@ def _near_tie(x, s, i):
 
 @pytest.mark.parametrize("flags", MODES)
 def test_decode_chain_full_size(decode_chain, flags):
-    """The 35-layer decode chain (245 GEMVs, 140 phases, 2.48 GB), every output of every GEMV.
+    """The 35-layer decode chain (245 GEMVs, 140 phases, 2.48 GB), every output of every GEMV
+    against the oracle.
 
-    A chain of quantised GEMVs is defined up to the int8 decisions of its hand-offs:
-    fp32 sums of a different order can move a block maximum or an element by an ulp,
-    and an element sitting on a rounding boundary (x/s = 94.5 exactly happens) then
-    rounds the other way - both decisions are correct, and from there on the two chains
-    quantise different vectors and part ways.  So:
-      1. up to the first link whose int8 input codes differ from the oracle's, every
-         output matches the oracle's chain within 1e-3;
-      2. at that link every differing code is off by one at a near-tie of the oracle's
-         own quantisation (a valid alternative decision, not a wrong value);
-      3. every link's output is the verified single-GEMV kernel's result on the vector
-         the link read (fp32 reassociation level), i.e. each link read the finished
-         output of the right earlier link and used the right weights."""
-    src, _, mats, x0, refs = decode_chain
+    Each link is one quantised GEMV of the vector it read (Gemma WebGPU Engine,
+    "Roadmap": each projection reads the buffer the previous one wrote), so every one of
+    the 245 outputs is compared, at 1e-3, with the oracle's GEMV of the same weights on
+    the fp32 vector the link actually read (the kernel's output of the link before, or
+    the external input).
+
+    The oracle's own end-to-end chain is a diagnostic beside it: a chain of quantised
+    GEMVs is defined up to the int8 decisions of its hand-offs (fp32 sums of another
+    order can move an element that sits on a rounding boundary to the other side; both
+    decisions are correct), so up to the first link whose int8 input codes differ from
+    the oracle chain's, every output also matches the oracle chain, and at that link
+    every differing code is off by one at a near-tie of the oracle's own quantisation."""
+    src, _, mats, x0, refs, ws_np = decode_chain
     _, ys, X = _decode_run(decode_chain, flags)
     torch.cuda.synchronize()
+    host = [y.cpu().numpy() for y in ys]
+    for j in range(len(src)):
+        x_read = x0 if src[j] < 0 else host[src[j]]
+        assert np.all(np.isfinite(x_read)), j
+        assert_close(host[j].astype(np.float64), _oracle_fn(ws_np[j], x_read))
     checked = 0
     for j in range(len(src)):
         x_dev = X if src[j] < 0 else ys[src[j]]
@@ -193,15 +199,9 @@ def test_decode_chain_full_size(decode_chain, flags):
                 assert abs(int(gq[i]) - int(oq[i])) == 1, (j, i)
                 assert _near_tie(x_or, os_, i) < 1e-3, (j, i, _near_tie(x_or, os_, i))
             break
-        assert_close(ys[j].cpu().numpy().astype(np.float64), refs[j])
+        assert_close(host[j].astype(np.float64), refs[j])
         checked += 1
     assert checked >= 14, f"only {checked} links before the first tie"  # at least two whole layers
-    for j in range(len(src)):
-        m = mats[j]
-        x_dev = X if src[j] < 0 else ys[src[j]]
-        single = qg.qgemv_q4(m["lo"], m["scale"], m["min"], x_dev)
-        e = oracle.normwise_error(ys[j].cpu().numpy(), single.cpu().numpy())
-        assert e < 1e-5, (j, e)
     assert qg.device_error() == 0
 
 

@@ -82,6 +82,43 @@ int ensure_smem_attr(const void* kernel, size_t smem, const LaunchCtx& lc) {
     return QG_OK;
 }
 
+// How many thread-block clusters of `cluster` CTAs (block threads, smem bytes of dynamic
+// shared memory each) can be resident on the device at once; cached per (kernel,
+// device, cluster, smem).  0 on failure.
+int max_active_clusters(const void* kernel, int cluster, int block, size_t smem, const LaunchCtx& lc) {
+    struct Entry {
+        const void* kernel;
+        int device, cluster, block;
+        size_t smem;
+        int count;
+    };
+    static Entry cache[64];
+    static int n = 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].kernel == kernel && cache[i].device == lc.device && cache[i].cluster == cluster &&
+            cache[i].block == block && cache[i].smem == smem)
+            return cache[i].count;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cluster * lc.sm_count));
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = (unsigned)cluster;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int count = 0;
+    if (cudaOccupancyMaxActiveClusters(&count, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (n < 64) cache[n++] = Entry{kernel, lc.device, cluster, block, smem, count};
+    return count;
+}
+
 static int check_weights(int bits, const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const uint16_t* min,
                          int n, int k) {
     if (bits != 2 && bits != 4 && bits != 6) return QG_ERR_UNSUPPORTED;

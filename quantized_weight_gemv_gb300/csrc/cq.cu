@@ -125,6 +125,157 @@ __global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
     }
 }
 
+// One group per row (k == group, G = 32*J, J >= 8): the transform is split over all
+// eight warps and each warp keeps several rows in flight.
+//  * Before griddepcontrol.wait each warp loads the packed indices of up to RPW of its
+//    rows into registers (lane l: the J/2 bytes of elements J*l .. J*l+J-1) and their
+//    scales: under programmatic dependent launch the weight reads overlap the preceding
+//    kernel's tail.
+//  * Transform: thread t holds elements E*t .. E*t+E-1 (E = J/8).  The butterflies over
+//    the low log2(E) index bits run in registers, the next five (the lane bits) through
+//    __shfl_xor_sync, and the top three (the warp bits) after one pass through shared
+//    memory, where each of 4J threads takes the eight elements c + 4J*m (m < 8) of one
+//    column c.  Its results, times 1/sqrt(G), go to the dot layout (element J*l + e at
+//    e*32 + l).
+//  * Each lane then holds its J transformed values in registers for all its rows: per
+//    row only the codebook look-ups (16 entries in 16 distinct banks: conflict-free for
+//    any index pattern) and the fused multiply-adds remain.
+template <int J>
+__global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
+    constexpr int G = 32 * J;
+    constexpr int E = J / 8;
+    constexpr int RPW = 4;                 // rows per warp loaded before the wait
+    constexpr int NWI = (J + 7) / 8;       // index words per lane and row
+    static_assert(J >= 8, "at least one element per thread");
+    extern __shared__ __align__(16) float sm[];
+    float* su = sm;       // [G], dot layout
+    float* sc = sm + G;   // [G], natural order (transform scratch)
+    __shared__ float scb[16];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int tw = gridDim.x * 8;
+    const int gw = blockIdx.x * 8 + wid;
+    const int my_rows = p.row_count > gw ? (p.row_count - gw + tw - 1) / tw : 0;
+    const size_t row_bytes = (size_t)(p.k >> 1);
+
+    uint32_t wi[RPW][NWI];
+    unsigned short sh[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        sh[i] = 0;
+#pragma unroll
+        for (int q = 0; q < NWI; ++q) wi[i][q] = 0u;
+        if (i < my_rows) {
+            const int r = p.row_start + gw + i * tw;
+            load_lane_indices<J>(p.idx + (size_t)r * row_bytes + (J / 2) * lane, wi[i]);
+            sh[i] = p.row_scale[r];
+        }
+    }
+    if (threadIdx.x < 16) scb[threadIdx.x] = half_bits_to_float(p.codebook[threadIdx.x]);
+
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+
+    // ---- transform: registers, lanes, then warps through shared memory
+    const int t = threadIdx.x;
+    float v[E];
+    if constexpr (E == 1) {
+        v[0] = p.x[t];
+    } else if constexpr (E == 2) {
+        const float2 a = reinterpret_cast<const float2*>(p.x)[t];
+        v[0] = a.x;
+        v[1] = a.y;
+    } else {
+        const float4 a = reinterpret_cast<const float4*>(p.x)[t];
+        v[0] = a.x;
+        v[1] = a.y;
+        v[2] = a.z;
+        v[3] = a.w;
+    }
+#pragma unroll
+    for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            if ((e & h) == 0) {
+                const float a = v[e], b = v[e + h];
+                v[e] = a + b;
+                v[e + h] = a - b;
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
+            v[e] = upper ? (o - v[e]) : (v[e] + o);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) sc[E * t + e] = v[e];
+    __syncthreads();
+    if (t < 4 * J) {
+        float u[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) u[m] = sc[t + 4 * J * m];
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                if ((m & h) == 0) {
+                    const float a = u[m], b = u[m + h];
+                    u[m] = a + b;
+                    u[m + h] = a - b;
+                }
+            }
+        }
+        // element i = t + 4J*m goes to (i % J) * 32 + i / J
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int i = t + 4 * J * m;
+            su[(i % J) * 32 + i / J] = u[m] * p.inv_sqrt_group;
+        }
+    }
+    __syncthreads();
+
+    float ul[J];
+#pragma unroll
+    for (int e = 0; e < J; ++e) ul[e] = su[e * 32 + lane];
+
+    // ---- the rows: codebook look-ups against the lane's transformed values
+    auto dot_row = [&](const uint32_t(&w)[NWI], unsigned short scale_h, int j) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int e = 0; e < J; ++e) {
+            const uint32_t c = (w[e >> 3] >> (4 * (e & 7))) & 15u;
+            acc = fmaf(scb[c], ul[e], acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) p.y[j] = half_bits_to_float(scale_h) * acc;
+    };
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+        if (i < my_rows) dot_row(wi[i], sh[i], gw + i * tw);
+    for (int i = RPW; i < my_rows; ++i) {
+        const int j = gw + i * tw;
+        const int r = p.row_start + j;
+        uint32_t w[NWI];
+        load_lane_indices<J>(p.idx + (size_t)r * row_bytes + (J / 2) * lane, w);
+        dot_row(w, p.row_scale[r], j);
+    }
+}
+
+template <int J>
+static int launch_cq_onegroup_t(const CqParams& p, const LaunchCtx& lc) {
+    auto kern = cq_onegroup_kernel<J>;
+    const size_t smem = (size_t)2 * 32 * J * sizeof(float);
+    if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
+    int grid = (p.row_count + 7) / 8;  // at least one row per warp
+    if (grid > lc.sm_count * 2) grid = lc.sm_count * 2;
+    if (grid < 1) grid = 1;
+    return launch_kernel(kern, dim3(grid), dim3(256), smem, lc, p);
+}
+
 template <int J>
 static int launch_cq_t(const CqParams& p, const LaunchCtx& lc) {
     auto kern = cq_kernel<J>;
@@ -138,6 +289,16 @@ static int launch_cq_t(const CqParams& p, const LaunchCtx& lc) {
 }
 
 int launch_cq(const CqParams& p, const LaunchCtx& lc) {
+    if (p.k == p.group) {
+        switch (p.group) {
+            case 256:
+                return launch_cq_onegroup_t<8>(p, lc);
+            case 512:
+                return launch_cq_onegroup_t<16>(p, lc);
+            case 1024:
+                return launch_cq_onegroup_t<32>(p, lc);
+        }
+    }
     switch (p.group) {
         case 128:
             return launch_cq_t<4>(p, lc);

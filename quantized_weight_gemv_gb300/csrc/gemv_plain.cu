@@ -188,8 +188,15 @@ __global__ void __launch_bounds__(512) read_floor_kernel(const uint4* __restrict
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+    // one atomic per CTA: same-address atomics from every warp would serialise in L2
+    __shared__ uint32_t sacc[16];
+    if ((threadIdx.x & 31) == 0) sacc[threadIdx.x >> 5] = acc;
+    __syncthreads();
     pdl_wait();
-    if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) acc ^= sacc[w];
+        atomicXor(out, acc);
+    }
 }
 
 int launch_read_floor(const void* src, size_t bytes, uint32_t* out, const LaunchCtx& lc) {

@@ -17,6 +17,10 @@ bool stream_supported(int bits, int n, int k, int batch, int epi) {
 int launch_stream(const StreamParams& p0, int bits, int epi, const LaunchCtx& lc) {
     if (!stream_supported(bits, p0.n, p0.k, p0.batch, epi)) return QG_ERR_UNSUPPORTED;
     StreamParams p = p0;
+    if (splitk_wanted(p.n, p.k, p.batch, epi)) {
+        const int rc = launch_splitk(p, bits, lc);
+        if (rc != QG_ERR_UNSUPPORTED) return rc;
+    }
     if (bits == 2) return launch_stream_bits<2>(p, epi, lc);
     return bits == 4 ? launch_stream_bits<4>(p, epi, lc) : launch_stream_bits<6>(p, epi, lc);
 }

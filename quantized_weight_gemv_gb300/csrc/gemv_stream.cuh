@@ -170,8 +170,8 @@ __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v
 // stage holds whole rows (5 in 240 blocks, or 10 in 480 for the 512-block Q2 stage) and
 // the rows, which straddle the lanes' block groups, are summed per lane and then
 // through one halving tree (GEN below).
-template <int BITS, int BC, int EPI, int NB>
-__global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(StreamParams p) {
+template <int BITS, int BC, int EPI, int NB, int W>
+__global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stream_kernel(StreamParams p) {
     constexpr int SB = stage_blocks<BITS, BC, NB>();  // blocks per stage (capacity)
     constexpr int JL = SB / 32;                        // blocks per lane per stage
     using SL = Slot<BITS, SB>;
@@ -194,7 +194,6 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int W = blockDim.x >> 5;
     const int D = p.stages;  // slots per warp
 
     // shared layout: slots[W][D] | full[W][D] | xq columns (16-byte aligned)
@@ -236,9 +235,46 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     }
     __syncwarp();
 
+    // stage t (in slot `slot_`, phase parity `phase_`) -> registers, then the slot refilled
+    // with stage t + D; false when the bounded wait ran out (warp-uniform)
+    uint4 cw[JU];
+    uint2 hw[JU];
+    unsigned short dh[JU], mh[JU];
+    auto fetch = [&](int t, int slot_, uint32_t phase_) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot_], phase_))) return false;
+        const unsigned char* st = slots + (size_t)slot_ * SL::BYTES;
+#pragma unroll
+        for (int j = 0; j < JU; ++j) {
+            const int fb = HALF ? (2 * (j / 3) + (lane >> 4)) * NB + 3 * (lane & 15) + j % 3 : lane + 32 * j;
+            if constexpr (BITS == 2) {
+                cw[j] = make_uint4(0u, 0u, 0u, 0u);
+                hw[j] = *reinterpret_cast<const uint2*>(st + 8 * fb);
+                mh[j] = 0;
+            } else {
+                cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
+                if constexpr (BITS == 6)
+                    hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
+                else
+                    hw[j] = make_uint2(0u, 0u);
+                mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
+            }
+            dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
+        }
+        __syncwarp();
+        if (lane == 0 && t + D < my_stages) {
+            fence_proxy_async();  // the slot's generic reads are done before the async refill
+            issue(t + D, slot_);
+        }
+        return true;
+    };
+    // 16-warp CTAs (a small share per SM): the first stage goes to registers and its slot
+    // is refilled before the wait below, one more stage per warp requested while the
+    // preceding kernel finishes.
+    const bool first_held = W == 16 && my_stages > 0 && fetch(0, 0, 0u);
+
     // ---- activation prologue (after the preceding kernel, which may have written x)
     pdl_wait();
-    quantize_x_cols<256>(p.x, p.k, p.batch, xqbase, xstride, threadIdx.x);
+    quantize_x_cols<W * 32>(p.x, p.k, p.batch, xqbase, xstride, threadIdx.x);
     __syncthreads();
 
     uint4 xl[BC][NXR], xh[BC][NXR];
@@ -272,7 +308,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     int slot = 0;
     uint32_t phase = 0;
     for (int t = 0; t < my_stages; ++t, slot = slot + 1 == D ? 0 : slot + 1, phase ^= slot == 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], phase))) {  // warp-uniform
+        if (!(t == 0 && first_held) && !fetch(t, slot, phase)) {
             atomicOr(p.err, ERR_WAIT_FULL);
             break;
         }
@@ -280,34 +316,6 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         const int part = t % PARTS;
         const long long row0 = r0 + (long long)u * R;
         const int rows_u = R == 1 ? 1 : min(R, nrows - u * R);
-        const unsigned char* st = slots + (size_t)slot * SL::BYTES;
-
-        // stage -> registers
-        uint4 cw[JU];
-        uint2 hw[JU];
-        unsigned short dh[JU], mh[JU];
-#pragma unroll
-        for (int j = 0; j < JU; ++j) {
-            const int fb = HALF ? (2 * (j / 3) + (lane >> 4)) * NB + 3 * (lane & 15) + j % 3 : lane + 32 * j;
-            if constexpr (BITS == 2) {
-                cw[j] = make_uint4(0u, 0u, 0u, 0u);
-                hw[j] = *reinterpret_cast<const uint2*>(st + 8 * fb);
-                mh[j] = 0;
-            } else {
-                cw[j] = *reinterpret_cast<const uint4*>(st + 16 * fb);
-                if constexpr (BITS == 6)
-                    hw[j] = *reinterpret_cast<const uint2*>(st + SL::HI + 8 * fb);
-                else
-                    hw[j] = make_uint2(0u, 0u);
-                mh[j] = *reinterpret_cast<const unsigned short*>(st + SL::MN + 2 * fb);
-            }
-            dh[j] = *reinterpret_cast<const unsigned short*>(st + SL::SC + 2 * fb);
-        }
-        __syncwarp();
-        if (lane == 0 && t + D < my_stages) {
-            fence_proxy_async();  // the slot's generic reads are done before the async refill
-            issue(t + D, slot);
-        }
 
         // block partials: part j of the lane belongs to row (lane + 32j) / NB of the stage.
         // In a stage of fewer than R rows the blocks past its last row are computed on
@@ -445,7 +453,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
     }
 
     if constexpr (EPI == EPI_ARGMAX) {
-        __shared__ ArgmaxPartial sred[8];
+        __shared__ ArgmaxPartial sred[W];
         __shared__ int sflag;
         argmax_finish(bv, bi, p.ws, p.argmax, sred, &sflag);
     } else if constexpr (EPI == EPI_SELECT) {
@@ -454,7 +462,7 @@ __global__ void __launch_bounds__(256, BC <= 2 ? 2 : 1) gemv_stream_kernel(Strea
         // log-sum-exp (NaN skipped) and the best (value, lowest id) among the allowed ids
         // that fall in the range, from one pass over the allowed list; the last CTA to
         // finish merges every CTA's partial.
-        __shared__ SelectPartial sred[8];
+        __shared__ SelectPartial sred[W];
         __shared__ int slast;
         __syncthreads();
         float m = -INFINITY, s = 0.0f;

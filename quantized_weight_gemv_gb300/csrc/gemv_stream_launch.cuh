@@ -14,16 +14,11 @@ inline int env_int(const char* name, int dflt) {
     return atoi(v);
 }
 
-template <int BITS, int BC, int EPI, int NB>
-int launch_t(StreamParams p, const LaunchCtx& lc) {
+template <int BITS, int BC, int EPI, int NB, int W>
+int launch_w(StreamParams p, const LaunchCtx& lc, int D, int per_sm) {
     using SL = Slot<BITS, stage_blocks<BITS, BC, NB>()>;
-    auto kern = gemv_stream_kernel<BITS, BC, EPI, NB>;
-    constexpr int W = 8;  // warps per CTA
+    auto kern = gemv_stream_kernel<BITS, BC, EPI, NB, W>;
     const size_t fixed = (size_t)BC * xq_stride(NB);
-    // Default: one ring slot per warp and two CTAs per SM (measured on GB300 as the
-    // fastest shape: a slot is refilled as soon as it has been copied to registers).
-    // QG_STREAM_SLOTS (slots per warp) and QG_STREAM_CTAS_PER_SM override it.
-    int D = env_int("QG_STREAM_SLOTS", 1);
     if (D < 1) D = 1;
     if (D > 8) D = 8;
     const size_t cap = (size_t)lc.max_smem_optin - 1024;  // room for static shared memory
@@ -36,7 +31,6 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
     p.stages = D;
     p.err = lc.err;
-    int per_sm = env_int("QG_STREAM_CTAS_PER_SM", BC <= 2 ? 2 : 1);
     if (per_sm < 1) per_sm = 1;
     int grid = lc.sm_count * per_sm;
     if (EPI == EPI_ARGMAX && grid > VOCAB_MAX_CTAS) grid = VOCAB_MAX_CTAS;
@@ -44,6 +38,41 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     if (grid > p.n) grid = p.n;
     if (grid < 1) grid = 1;
     return launch_kernel(kern, dim3(grid), dim3(W * 32), smem, lc, p);
+}
+
+template <int BITS, int BC, int EPI, int NB>
+int launch_t(StreamParams p, const LaunchCtx& lc) {
+    constexpr int SB = stage_blocks<BITS, BC, NB>();
+    constexpr int R = NB >= SB ? 1 : SB / NB;
+    constexpr int PARTS = NB > SB ? NB / SB : 1;
+    // Default: 8 warps per CTA, two CTAs per SM (one from four columns), one ring slot
+    // per warp: a slot is refilled as soon as it has been copied to registers, and the
+    // stream of a large matrix keeps every warp busy (measured on GB300 as the fastest
+    // shape for the vocabulary heads and the large projections).
+    // A single GEMV whose share per SM is one to four stages per warp of one 16-warp CTA
+    // (for 16384 x 2048: 27 stages of 5 KB per SM) takes that CTA instead, with enough
+    // slots that every stage of every warp is requested before the kernel waits for the
+    // preceding work (one stage in registers, the rest in slots): the weight stream then
+    // overlaps the preceding kernel's tail and the activation prologue.
+    // QG_STREAM_WARPS (8 or 16), QG_STREAM_SLOTS and QG_STREAM_CTAS_PER_SM override it.
+    int W = 8, D = 1, per_sm = BC <= 2 ? 2 : 1;
+    if constexpr (BC == 1 && EPI == EPI_STORE) {
+        const long long rows = ((long long)p.n + lc.sm_count - 1) / lc.sm_count;
+        const long long stages = (NB >= SB ? rows : (rows + R - 1) / R) * PARTS;
+        const long long per_warp = (stages + 15) / 16;
+        if (stages >= 16 && per_warp <= 4) {
+            W = 16;
+            per_sm = 1;
+            D = per_warp > 1 ? (int)per_warp - 1 : 1;
+        }
+        W = env_int("QG_STREAM_WARPS", W) == 16 ? 16 : 8;
+    }
+    D = env_int("QG_STREAM_SLOTS", D);
+    per_sm = env_int("QG_STREAM_CTAS_PER_SM", per_sm);
+    if constexpr (BC == 1 && EPI == EPI_STORE) {
+        if (W == 16) return launch_w<BITS, BC, EPI, NB, 16>(p, lc, D, per_sm);
+    }
+    return launch_w<BITS, BC, EPI, NB, 8>(p, lc, D, per_sm);
 }
 
 template <int BITS, int BC, int EPI>

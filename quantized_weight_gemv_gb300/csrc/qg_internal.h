@@ -67,9 +67,12 @@ struct LaunchCtx {
     int sm_count;
     int max_smem_optin;
     unsigned int* err;  // device address of the error word
+    int cluster = 1;    // thread-block cluster size of the launch (1: none)
 };
 
 int ensure_smem_attr(const void* kernel, size_t smem, const LaunchCtx& lc);
+// resident clusters of `cluster` CTAs at once (cudaOccupancyMaxActiveClusters, cached); 0 on failure
+int max_active_clusters(const void* kernel, int cluster, int block, size_t smem, const LaunchCtx& lc);
 
 template <typename... KArgs, typename... Args>
 int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, const LaunchCtx& lc, Args... args) {
@@ -78,12 +81,23 @@ int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, 
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = lc.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
     if (lc.flags & QG_FLAG_PDL) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (lc.cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)lc.cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (na) {
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = na;
     }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
     if (e != cudaSuccess) {
@@ -97,6 +111,9 @@ int launch_plain(const PlainParams& p, int bits, int epi, const LaunchCtx& lc);
 // returns QG_ERR_UNSUPPORTED when the shape has no bulk-copy variant
 int launch_stream(const StreamParams& p, int bits, int epi, const LaunchCtx& lc);
 bool stream_supported(int bits, int n, int k, int batch, int epi);
+// split-K streaming for short-N / long-K single GEMVs (gemv_splitk.cu)
+bool splitk_wanted(int n, int k, int batch, int epi);
+int launch_splitk(const StreamParams& p, int bits, const LaunchCtx& lc);
 int launch_cq(const CqParams& p, const LaunchCtx& lc);
 // tensor-core small-batch MMVQ (Q4, batch 8..16)
 bool mma_supported(int bits, int k, int batch);

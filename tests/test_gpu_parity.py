@@ -627,3 +627,50 @@ def test_logits_select_infinities():
         assert int(tok.item()) == ref_tok
         got = float(lp.item())
         assert (np.isnan(got) and np.isnan(ref_lp)) or got == ref_lp == -np.inf or abs(got - ref_lp) < 1e-9, (got, ref_lp)
+
+
+# ---------------------------------------------------------------- split-K (short N, long K)
+@pytest.mark.parametrize("bits", [2, 4, 6])
+@pytest.mark.parametrize("k", [4096, 8192, 16384])
+@pytest.mark.parametrize("n", [1, 5, 37, 300, 2048, 8192])
+def test_gemv_split_k(bits, n, k):
+    """Long activations and at most 8192 rows take the split-K kernel (clusters of k/2048
+    CTAs, each one k slice, partial sums added in slice order through distributed shared
+    memory): ragged row ranges per cluster, one row, more clusters than rows."""
+    w = datagen.make_quantized(bits, 11 * n + k + bits, n, k)
+    x = datagen.normal_f32(11 * n + k + bits, 1, k)
+    wd = dev_w(w)
+    ref = oracle_gemv_par(w, x) if n * k >= (1 << 24) else oracle.gemv(w, x)
+    for flags in (0, qg.QG_FLAG_PDL):
+        y = gpu_gemv(wd, x, flags)
+        assert_close(y, ref)
+    # deterministic: the slice order of the sum is fixed
+    assert np.array_equal(gpu_gemv(wd, x), gpu_gemv(wd, x))
+
+
+def test_gemv_split_k_down_projection_as_benched():
+    """The decode stream's down projection (2048 x 16384, layer 0) as one call per matrix,
+    24 back-to-back PDL calls in a CUDA graph (as timed), against the oracle."""
+    from datagen import workloads as W
+    w, x = W.decode_projection(0, 6)
+    wd = dev_w(w)
+    xt = torch.from_numpy(x).to(DEV)
+    ref = oracle_gemv_par(w, x)
+    ys = [torch.full((2048,), float("nan"), device=DEV) for _ in range(24)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for y in ys:
+            qg.qgemv_q4(wd["lo"], wd["scale"], wd["min"], xt, y=y, flags=qg.QG_FLAG_PDL)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for y in ys:
+            qg.qgemv_q4(wd["lo"], wd["scale"], wd["min"], xt, y=y, flags=qg.QG_FLAG_PDL)
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    first = ys[0].cpu().numpy()
+    assert_close(first.astype(np.float64), ref)
+    for y in ys[1:]:
+        assert np.array_equal(y.cpu().numpy(), first)

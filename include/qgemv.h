@@ -83,8 +83,10 @@ int qg_version(void);
  * give up after a bounded time and record a nonzero code here instead of hanging:
  * 1 a weight tile never landed, 2 a ring slot was never freed (qgemv_chain's
  * producer), 4 a copy in flight never landed while stopping, 8 a grid-wide barrier
- * of qgemv_chain ran out.  Reads and clears the word of the
- * current device; synchronises the device.
+ * of qgemv_chain ran out, 16 a CTA of qgemv_chain's persistent kernel stopped at a
+ * phase boundary because the chain's abort word was set (by a CTA whose wait ran
+ * out, or before the call).  Reads and clears the word of the current device;
+ * synchronises the device.
  * Returns QG_OK or QG_ERR_CUDA; *code receives the word (0 = no error).
  */
 int qg_device_error(uint32_t* code);

@@ -248,18 +248,20 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned int* p) {
 }
 
 // Thread 0 of each CTA: arrive, then wait until `target` arrivals (all CTAs of this
-// and every earlier boundary).  False when the wait ran out or another CTA gave up.
+// and every earlier boundary).  False when the wait ran out (ERR_WAIT_GRID, and the abort
+// word set for the others) or the abort word is set (ERR_ABORTED): the abort word is read
+// before every look at the count, so once it is set no CTA passes another boundary.
 __device__ bool grid_barrier(const CParams& p, unsigned target) {
     // release: the CTA's outputs (ordered before by the consumers' barrier) before the arrival
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.ctl) : "memory");
-    if (ld_acquire_gpu(p.ctl) >= target) return true;
     const unsigned long long t0 = globaltimer_ns();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-            if (ld_acquire_gpu(p.ctl) >= target) return true;
-        if (ld_acquire_gpu(p.ctl + 1) != 0u) return false;
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+    for (int spin = 0;; ++spin) {
+        if (ld_acquire_gpu(p.ctl + 1) != 0u) {
+            atomicOr(p.err, ERR_ABORTED);
+            return false;
+        }
+        if (ld_acquire_gpu(p.ctl) >= target) return true;
+        if ((spin & 15) == 15 && globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
             atomicOr(p.err, ERR_WAIT_GRID);
             atomicExch(p.ctl + 1, 1u);
             return false;

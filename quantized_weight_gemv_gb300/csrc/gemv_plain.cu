@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
                     if (c < p.batch) p.y[(size_t)c * p.n + r] = acc[c];
             }
         } else {
-            const float l = softcap_apply(acc[0], p.softcap);
+            const float l = softcap_apply(acc[0], p.softcap, softcap_inv(p.softcap));
             if (lane == 0 && p.y) p.y[r] = l;
             if (better(l, r, bv, bi)) {
                 bv = l;

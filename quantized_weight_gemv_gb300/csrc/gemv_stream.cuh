@@ -147,15 +147,15 @@ __host__ __device__ constexpr size_t xq_offset(int nslots, int slot_bytes) {
 
 template <int EPI, int BC>
 __device__ __forceinline__ void emit_row(const StreamParams& p, long long row, const float (&v)[BC], float& bv,
-                                         int& bi) {
+                                         int& bi, float inv_c) {
     if constexpr (EPI == EPI_STORE) {
 #pragma unroll
         for (int c = 0; c < BC; ++c)
             if (c < p.batch) p.y[(size_t)c * p.n + row] = v[c];
     } else if constexpr (EPI == EPI_SELECT) {
-        p.y[row] = softcap_apply(v[0], p.softcap);  // folded into the selection at the CTA's end
+        p.y[row] = softcap_apply(v[0], p.softcap, inv_c);  // folded into the selection at the CTA's end
     } else {
-        const float l = softcap_apply(v[0], p.softcap);
+        const float l = softcap_apply(v[0], p.softcap, inv_c);
         if (p.y) p.y[row] = l;
         if (better(l, (int)row, bv, bi)) {
             bv = l;
@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
 
     float bv = __int_as_float(0x7fc00000);
     int bi = 0x7fffffff;
+    const float inv_c = softcap_inv(p.softcap);
     float rowacc[BC];  // running sum of a row that spans several stages
 #pragma unroll
     for (int c = 0; c < BC; ++c) rowacc[c] = 0.0f;
@@ -362,7 +363,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                 float out[BC];
 #pragma unroll
                 for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+                emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
             }
         } else if constexpr (GEN) {
             // rows straddle the lanes' block groups: block l + 32j of lane l lies in row
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                     float out[BC];
 #pragma unroll
                     for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
                 }
             }
         } else if constexpr (NB >= 32) {
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                         float out[BC];
 #pragma unroll
                         for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                        emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+                        emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
                     }
                 }
             }
@@ -446,7 +447,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                     float out[BC];
 #pragma unroll
                     for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi);
+                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
                 }
             }
         }

@@ -10,8 +10,10 @@
 namespace qg {
 
 // Codes OR-ed into the device error word (its address is a kernel parameter) by a
-// kernel whose bounded wait ran out.  Host side: qg_device_error() reads and clears it.
-enum : unsigned { ERR_WAIT_FULL = 1u, ERR_WAIT_EMPTY = 2u, ERR_WAIT_DRAIN = 4u, ERR_WAIT_GRID = 8u };
+// kernel whose bounded wait ran out (1, 2, 4, 8), or by a CTA of the persistent chain
+// that stopped on the chain's abort word (16).  Host side: qg_device_error() reads and
+// clears it.
+enum : unsigned { ERR_WAIT_FULL = 1u, ERR_WAIT_EMPTY = 2u, ERR_WAIT_DRAIN = 4u, ERR_WAIT_GRID = 8u, ERR_ABORTED = 16u };
 
 constexpr int WARP = 32;
 // 1 s: far beyond any legitimate wait of these kernels, short enough to keep the context alive.
@@ -265,8 +267,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------- soft-cap + argmax ordering
-__device__ __forceinline__ float softcap_apply(float z, float c) {
-    return c > 0.0f ? c * tanhf(__fdiv_rn(z, c)) : z;
+// l = c * tanh(z / c) (c > 0; c <= 0: no cap), z / c taken as z times inv_c = the
+// correctly rounded 1/c, computed once per kernel (within an ulp of the quotient)
+__device__ __forceinline__ float softcap_inv(float c) { return c > 0.0f ? __frcp_rn(c) : 0.0f; }
+__device__ __forceinline__ float softcap_apply(float z, float c, float inv_c) {
+    return c > 0.0f ? c * tanhf(z * inv_c) : z;
 }
 
 // (value, index) order for the argmax: larger value first, then lower index; NaN never wins.

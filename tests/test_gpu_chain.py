@@ -224,22 +224,27 @@ def test_decode_chain_modes_identical_and_equivariant(decode_chain):
 
 
 def test_chain_abort_word_stops_and_rearms():
-    """Persistent kernel: a set abort word makes every CTA stop at its next phase boundary without waiting
-    out the barrier; the workspace comes back zero and the next call is correct."""
+    """Persistent kernel: a set abort word makes every CTA stop at its next phase boundary
+    without waiting out the barrier - no output of a phase after the first is written by
+    any CTA, and the device error word records the stop (16) - the workspace comes back
+    zero and the next call is correct."""
     n = 2048
     ws_np = [datagen.make_quantized(4, 800 + i, n, n) for i in range(4)]
     mats = [dev_w(w) for w in ws_np]
     x0 = datagen.normal_f32(80, 1, n)
     X = torch.from_numpy(x0).to(DEV)
-    ys = [torch.empty(n, device=DEV) for _ in range(4)]
+    ys = [torch.full((n,), float("nan"), device=DEV) for _ in range(4)]
     ch = qg.ChainGemv(4, mats, [X, ys[0], ys[1], ys[2]], ys, [1, 1, 1, 1], flags=qg.QG_FLAG_CHAIN_PERSISTENT)
+    assert qg.device_error() == 0
     ctl = ch.ws[:qg.QG_CHAIN_CTL_BYTES].view(torch.int32)
     ctl[1] = 1
     torch.cuda.synchronize()
     ch.run()
     torch.cuda.synchronize()
+    for y in ys[1:]:  # every CTA stopped at the first boundary
+        assert bool(torch.isnan(y).all())
     assert int(ch.ws[:qg.QG_CHAIN_CTL_BYTES].count_nonzero()) == 0
-    assert qg.device_error() == 0
+    assert qg.device_error() == 16
     ch.run()
     refs = oracle.gemv_chain(ws_np, [-1, 0, 1, 2], [x0])
     for y, r in zip(ys, refs):

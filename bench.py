@@ -72,6 +72,7 @@ CASES = {
     "q4_batched_b8_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
     "cq_8192x512": None,  # the CQ matvec, 64 rotating copies (run_cq_case)
+    "read_floor_20971520B": None,  # the plain-read floor hook over 8 rotating 21 MB buffers (run_floor_case)
     "select_262144": None,  # constrained selection over 262144 logits, 1 % allowed (run_select_case)
     "q4_chain_persistent": None,  # the decode chain, --layers layers (run_chain_case)
     "q4_chain_launches": None,
@@ -153,6 +154,28 @@ def run_cq_case(args):
                       "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
 
 
+def run_floor_case(args):
+    """Profiling case: the plain-read floor hook over 8 rotating buffers of 20,971,520 bytes
+    (one 16384 x 2048 Q4 matrix's bytes), --reps rounds."""
+    import torch
+
+    import quantized_weight_gemv_gb300 as qg
+
+    device = torch.device("cuda", 0)
+    nbytes = 20971520
+    bufs = [torch.empty(nbytes, dtype=torch.uint8, device=device).fill_(i) for i in range(8)]
+    acc = torch.zeros(1, dtype=torch.int32, device=device)
+    state = {"i": 0}
+
+    def call():
+        qg.qg_read_floor(bufs[state["i"] % 8], out=acc)
+        state["i"] += 1
+
+    ms = time_eager(call, torch.cuda.current_stream(device), args.reps * 8)
+    print(json.dumps({"case": args.case, "calls": args.reps * 8, "us_per_call_eager": ms * 1e3,
+                      "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
+
+
 def run_select_case(args):
     """Profiling case: constrained selection over 262144 seeded logits with the benchmark's
     allowed list (about 1 % of the ids), --reps calls."""
@@ -185,6 +208,8 @@ def run_case(args):
         return run_cq_case(args)
     if args.case == "select_262144":
         return run_select_case(args)
+    if args.case == "read_floor_20971520B":
+        return run_floor_case(args)
 
     import quantized_weight_gemv_gb300 as qg
     from datagen import workloads as W

@@ -188,7 +188,9 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
     // distinct activation blocks per lane.  GEN (48 blocks per row): lane l meets blocks
     // (l + 32j) mod 48, and 96 = 0 mod 48, so only the three of j mod 3
     constexpr int NXB = GEN ? 3 : NB >= 32 ? (NB < SB ? NB / 32 : JL) : 1;
-    constexpr bool XREG = NB <= 128 && BC * NXB <= 8;  // activation words in registers
+    // activation words in registers, except for four columns of rows of 64+ blocks, whose
+    // 80 registers of words would leave room for only one 8-warp CTA per SM
+    constexpr bool XREG = NB <= 128 && BC * NXB <= (BC == 4 ? 4 : 8);
     constexpr int NXR = XREG ? NXB : 1;
     static_assert(!GEN || NB == 48, "blocks per row: a power of two, or 48");
 

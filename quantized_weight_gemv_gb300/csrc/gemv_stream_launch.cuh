@@ -56,7 +56,7 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     // overlaps the preceding kernel's tail and the activation prologue.
     // QG_STREAM_WARPS (8 or 16), QG_STREAM_SLOTS and QG_STREAM_CTAS_PER_SM override it.
     int W = 8, D = 1, per_sm = BC <= 2 ? 2 : 1;
-    if constexpr (BC <= 2 && EPI == EPI_STORE) {
+    if constexpr (BC <= 4 && EPI == EPI_STORE) {
         const long long rows = ((long long)p.n + lc.sm_count - 1) / lc.sm_count;
         const long long stages = (NB >= SB ? rows : (rows + R - 1) / R) * PARTS;
         const long long per_warp = (stages + 15) / 16;
@@ -69,7 +69,7 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     }
     D = env_int("QG_STREAM_SLOTS", D);
     per_sm = env_int("QG_STREAM_CTAS_PER_SM", per_sm);
-    if constexpr (BC <= 2 && EPI == EPI_STORE) {
+    if constexpr (BC <= 4 && EPI == EPI_STORE) {
         if (W == 16) return launch_w<BITS, BC, EPI, NB, 16>(p, lc, D, per_sm);
     }
     return launch_w<BITS, BC, EPI, NB, 8>(p, lc, D, per_sm);

@@ -64,6 +64,10 @@ CASES = {
     "q4_single_1024x1024": (4, 1024, 1024, 512),
     "q4_gate_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b2_16384x2048": (4, 16384, 2048, 8),
+    "q4_batched_b4_2048x2048": (4, 2048, 2048, 64),
+    "q4_plain_16384x2048": (4, 16384, 2048, 8),  # the plain-load kernel (QG_FLAG_PLAIN)
+    "q2_gemv_262144x1536": (2, 262144, 1536, 2),  # qgemv_q2 (no soft-cap, no argmax)
+    "q6_vocab_select_262144x2048": (6, 262144, 2048, 1),  # soft-cap + constrained selection, one launch
     "q4_down_2048x16384": (4, 2048, 16384, 8),
     "q4_q_2048x2048": (4, 2048, 2048, 64),
     "q6_vocab_262144x2048": (6, 262144, 2048, 1),
@@ -227,12 +231,24 @@ def run_case(args):
         ws = qg.vocab_workspace(device)
         am = torch.empty(1, dtype=torch.int32, device=device)
     fl = qg.QG_FLAG_PDL if args.graph else 0
+    if "_plain_" in args.case:
+        fl |= qg.QG_FLAG_PLAIN
+    if "_select_" in args.case:
+        allowed = torch.from_numpy(W.select_allowed(n)).to(device)
+        tok = torch.empty(1, dtype=torch.int32, device=device)
+        lp = torch.empty(1, dtype=torch.float32, device=device)
+        vws = qg.vocab_select_workspace(device)
 
     def call(r):
         if batch > 1:
             qg.qgemv_batched(4, r["lo"], None, r["scale"], r["min"], x, Y=y, flags=fl)
         elif bits == 4:
             qg.qgemv_q4(r["lo"], r["scale"], r["min"], x[0], y=y[0], flags=fl)
+        elif "_gemv_" in args.case:
+            qg.qgemv_q2(r["lo"], r["scale"], x[0], y=y[0], flags=fl)
+        elif "_select_" in args.case:
+            qg.vocab_softcap_select(bits, r["lo"], r.get("hi"), r["scale"], r.get("min"), x[0], W.SOFTCAP,
+                                    allowed=allowed, logits=y[0], token=tok, logprob=lp, ws=vws, flags=fl)
         else:
             qg.vocab_softcap_argmax(bits, r["lo"], r.get("hi"), r["scale"], r.get("min"), x[0], W.SOFTCAP,
                                     logits=y[0], argmax=am, ws=ws, flags=fl)

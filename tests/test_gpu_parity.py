@@ -674,3 +674,21 @@ def test_gemv_split_k_down_projection_as_benched():
     assert_close(first.astype(np.float64), ref)
     for y in ys[1:]:
         assert np.array_equal(y.cpu().numpy(), first)
+
+
+# ---------------------------------------------------------------- 16-warp, whole-share-in-flight layout
+@pytest.mark.parametrize("bits", [2, 4, 6])
+@pytest.mark.parametrize("n,k", [(12345, 2048), (16384 + 77, 2048), (30001, 1024), (15003, 1536), (9300, 2048)])
+@pytest.mark.parametrize("batch", [1, 2, 4])
+def test_gemv_sixteen_warp_layout(bits, n, k, batch):
+    """Shapes whose share per SM is 16 to 64 stages take one 16-warp CTA per SM with the
+    first stage fetched before the dependency wait: ragged last stages and row ranges, one
+    to four columns (four columns read their activation words from shared memory)."""
+    w = datagen.make_quantized(bits, 13 * n + k + batch, n, k)
+    X = datagen.normal_f32(13 * n + k + batch, 1, batch * k).reshape(batch, k)
+    wd = dev_w(w)
+    Xt = torch.from_numpy(X).to(DEV)
+    for flags in (0, qg.QG_FLAG_PDL):
+        Y = qg.qgemv_batched(bits, wd["lo"], wd.get("hi"), wd["scale"], wd["min"], Xt, flags=flags).cpu().numpy()
+        for b in range(batch):
+            assert_close(Y[b].astype(np.float64), oracle_gemv_par(w, X[b]))

@@ -114,58 +114,77 @@ __host__ __device__ constexpr int xq_bytes(int nb) { return 40 * nb; }
 
 // Cooperative quantisation of `batch` activation columns x[c][k] into per-column
 // XqViews (column c at base + c * stride) by NT threads (t = 0..NT-1, whole warps).
-// The float4s of all columns form one index space; thread t takes number i*NT + t,
-// so eight consecutive lanes hold one block of 32 of one column and a block's max
-// and sum need three shuffles.  All CHUNK loads of a round are issued before any is
-// used, so the prologue costs about one L2 round trip per CHUNK*NT float4s.
+// The columns' runs of V consecutive values (V = 4 or 8) form one index space; thread
+// t takes run i*NT + t, so 32/V consecutive lanes hold one block of 32 of one column
+// and a block's max and sum take log2(32/V) shuffles.  All CHUNK loads of a round are
+// issued before any is used, so the prologue costs about one L2 round trip per round.
 // L2ONLY reads x with ld.global.cg: for a vector other SMs wrote during the same
 // launch, which the non-coherent (and L1) path may hold stale.  (What a preceding
 // kernel wrote is visible to every read issued after griddepcontrol.wait.)
-template <int NT, bool L2ONLY = false>
-__device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int k, int batch, unsigned char* base,
-                                                int stride, int t) {
-    constexpr int CHUNK = 8;
+template <int NT, bool L2ONLY, int V>
+__device__ __forceinline__ void quantize_runs(const float* __restrict__ x, int k, int batch, unsigned char* base,
+                                              int stride, int t) {
+    constexpr int F = V / 4;         // float4s per run
+    constexpr int CHUNK = 8 / F;     // runs per thread per round (8 float4 loads in flight)
+    constexpr int LPB = 32 / V;      // lanes per block
     const int nb = k >> 5;
-    const int nf4 = k >> 2;  // a multiple of 8
-    const int total = batch * nf4;
-    const int m = t & 7;     // float4 index within the block
+    const int nrun = k / V;          // runs per column
+    const int total = batch * nrun;
+    const int m = t & (LPB - 1);     // run within the block
     const float4* x4 = reinterpret_cast<const float4*>(x);
     for (int r0 = 0; r0 < total; r0 += NT * CHUNK) {
-        float4 r[CHUNK];
+        float4 r[CHUNK][F];
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
             const int idx = r0 + i * NT + t;
-            r[i] = idx < total ? (L2ONLY ? __ldcg(x4 + idx) : __ldg(x4 + idx)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int f = 0; f < F; ++f)
+                r[i][f] = idx < total ? (L2ONLY ? __ldcg(x4 + F * idx + f) : __ldg(x4 + F * idx + f))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
             if (r0 + i * NT >= total) break;  // the same for every thread: nothing left in this round
             const int idx = r0 + i * NT + t;
-            float a = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            float a = 0.0f;
+#pragma unroll
+            for (int f = 0; f < F; ++f)
+                a = fmaxf(a, fmaxf(fmaxf(fabsf(r[i][f].x), fabsf(r[i][f].y)), fmaxf(fabsf(r[i][f].z), fabsf(r[i][f].w))));
+#pragma unroll
+            for (int o = 1; o < LPB; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
             const float s = __fdiv_rn(a, 127.0f);
-            int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+            int q[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) q[e] = 0;
             if (s != 0.0f) {
                 const float inv = __frcp_rn(s);
-                q0 = quant_code(r[i].x, s, inv);
-                q1 = quant_code(r[i].y, s, inv);
-                q2 = quant_code(r[i].z, s, inv);
-                q3 = quant_code(r[i].w, s, inv);
+#pragma unroll
+                for (int f = 0; f < F; ++f) {
+                    q[4 * f + 0] = quant_code(r[i][f].x, s, inv);
+                    q[4 * f + 1] = quant_code(r[i][f].y, s, inv);
+                    q[4 * f + 2] = quant_code(r[i][f].z, s, inv);
+                    q[4 * f + 3] = quant_code(r[i][f].w, s, inv);
+                }
             }
-            int S = q0 + q1 + q2 + q3;
-            S += __shfl_xor_sync(0xffffffffu, S, 1);
-            S += __shfl_xor_sync(0xffffffffu, S, 2);
-            S += __shfl_xor_sync(0xffffffffu, S, 4);
+            int S = 0;
+            uint32_t packed[F];
+#pragma unroll
+            for (int f = 0; f < F; ++f) {
+                S += (q[4 * f] + q[4 * f + 1]) + (q[4 * f + 2] + q[4 * f + 3]);
+                packed[f] = (uint32_t)(q[4 * f] & 255) | ((uint32_t)(q[4 * f + 1] & 255) << 8) |
+                            ((uint32_t)(q[4 * f + 2] & 255) << 16) | ((uint32_t)(q[4 * f + 3] & 255) << 24);
+            }
+#pragma unroll
+            for (int o = 1; o < LPB; o <<= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
             if (idx < total) {
-                const int c = idx / nf4;
-                const int b = (idx - c * nf4) >> 3;
+                const int c = batch == 1 ? 0 : idx / nrun;  // (no division for one column)
+                const int b = (idx - c * nrun) / LPB;
                 const XqView v = xq_view(base + (size_t)c * stride, nb);
-                const uint32_t packed = (uint32_t)(q0 & 255) | ((uint32_t)(q1 & 255) << 8) |
-                                        ((uint32_t)(q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
-                int8_t* dst = m < 4 ? v.lo + 16 * b + 4 * m : v.hi + 16 * b + 4 * (m - 4);
-                *reinterpret_cast<uint32_t*>(dst) = packed;
+                int8_t* dst = m < LPB / 2 ? v.lo + 16 * b + V * m : v.hi + 16 * b + V * (m - LPB / 2);
+                if constexpr (F == 2)
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+                else
+                    *reinterpret_cast<uint32_t*>(dst) = packed[0];
                 if (m == 0) {
                     v.s[b] = s;
                     v.S[b] = (float)S;
@@ -173,6 +192,17 @@ __device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int
             }
         }
     }
+}
+
+// Runs of 8 values when every thread gets at least one (the scale, its reciprocal
+// and the shuffles then serve 8 values), else runs of 4 (more threads in the one round).
+template <int NT, bool L2ONLY = false>
+__device__ __forceinline__ void quantize_x_cols(const float* __restrict__ x, int k, int batch, unsigned char* base,
+                                                int stride, int t) {
+    if (batch * k >= 8 * NT)
+        quantize_runs<NT, L2ONLY, 8>(x, k, batch, base, stride, t);
+    else
+        quantize_runs<NT, L2ONLY, 4>(x, k, batch, base, stride, t);
 }
 
 // ---------------------------------------------------------------- dp4a block dots

@@ -299,3 +299,62 @@ def test_chain_in_cuda_graph(flags):
     refs = oracle.gemv_chain(ws_np, [s_ for _, _, s_ in spec], ext, _oracle_fn)
     for y, r in zip(ys, refs):
         assert_close(y.cpu().numpy().astype(np.float64), r)
+
+
+def _random_reuse_chain(rng, pool_n, n_buf):
+    """Phases over a pool of reused buffers: (n, k, x buffer, y buffer) per GEMV and the
+    phase sizes; within a phase no output overlaps another output or an input."""
+    spec, sizes = [], []
+    for _ in range(rng.randint(2, 7)):
+        used_out, ins, phase, inputs = [], [], [], set()
+        for _ in range(rng.randint(1, 4)):
+            k = rng.choice([1024, 2048, 4096, 16384])
+            n = rng.choice([256, 512, 2048])
+            xi = rng.choice([b for b in range(n_buf) if b not in used_out])
+            if sum(kk for _, kk in inputs | {(xi, k)}) > 32768:  # distinct inputs of a phase
+                break
+            inputs.add((xi, k))
+            outs = [b for b in range(n_buf) if b not in used_out and b not in ins and b != xi]
+            if not outs:
+                break
+            yi = rng.choice(outs)
+            ins.append(xi)
+            used_out.append(yi)
+            phase.append((n, k, xi, yi))
+        if phase and not any(o in ins for o in used_out):
+            spec += phase
+            sizes.append(len(phase))
+    return spec, sizes
+
+
+@pytest.mark.parametrize("flags", MODES)
+def test_chain_reused_buffers_match_phase_by_phase(flags):
+    """Random chains whose phases read, overwrite and reuse a small pool of buffers (a
+    later phase may overwrite what an earlier one read, or write where an earlier one
+    wrote): the chain leaves every buffer bit-identical to running the phases one by one
+    as separate qgemv_grouped calls with a device synchronisation between them."""
+    import random
+
+    rng = random.Random(77)
+    pool_n, n_buf = 16384, 6
+    for trial in range(16):
+        spec, sizes = _random_reuse_chain(rng, pool_n, n_buf)
+        init = torch.from_numpy(np.stack([datagen.normal_f32(900 + trial, b, pool_n) for b in range(n_buf)])).to(DEV)
+        mats = [dev_w(datagen.make_quantized(4, 5000 + 100 * trial + i, n, k)) for i, (n, k, _, _) in enumerate(spec)]
+
+        def views(pool):
+            return ([pool[xi, :k] for (n, k, xi, yi) in spec], [pool[yi, :n] for (n, k, xi, yi) in spec])
+
+        pa = init.clone()
+        xa, ya = views(pa)
+        qg.ChainGemv(4, mats, xa, ya, sizes, flags=flags).run()
+        pb = init.clone()
+        xb, yb = views(pb)
+        off = 0
+        for m in sizes:
+            qg.qgemv_grouped(4, mats[off:off + m], xb[off:off + m], yb[off:off + m])
+            torch.cuda.synchronize()
+            off += m
+        torch.cuda.synchronize()
+        assert torch.equal(pa, pb), (trial, sizes)
+    assert qg.device_error() == 0

@@ -14,6 +14,9 @@
 // bits run in registers, those over the lane bits through __shfl_xor_sync.  The
 // result is kept in shared memory transposed (element J*l + j at j*32 + l), so
 // that in the dot loop lane l reads its J values without bank conflicts.
+#include <type_traits>
+
+#include "gemv_stream.cuh"  // stream::halving_reduce
 #include "qg_internal.h"
 
 namespace qg {
@@ -142,14 +145,14 @@ __global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
 //    any index pattern) and the fused multiply-adds remain.
 template <int J>
 __global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
-    constexpr int G = 32 * J;
     constexpr int E = J / 8;
     constexpr int RPW = 4;                 // rows per warp loaded before the wait
     constexpr int NWI = (J + 7) / 8;       // index words per lane and row
     static_assert(J >= 8, "at least one element per thread");
     extern __shared__ __align__(16) float sm[];
-    float* su = sm;       // [G], dot layout
-    float* sc = sm + G;   // [G], natural order (transform scratch)
+    constexpr int SU = 33;  // row stride of the dot layout (32 + 1: conflict-free scatter)
+    float* su = sm;           // [J][SU], dot layout
+    float* sc = sm + J * SU;  // [32 J], natural order (transform scratch)
     __shared__ float scb[16];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int tw = gridDim.x * 8;
@@ -233,29 +236,52 @@ __global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int i = t + 4 * J * m;
-            su[(i % J) * 32 + i / J] = u[m] * p.inv_sqrt_group;
+            su[(i % J) * SU + i / J] = u[m] * p.inv_sqrt_group;
         }
     }
     __syncthreads();
 
     float ul[J];
 #pragma unroll
-    for (int e = 0; e < J; ++e) ul[e] = su[e * 32 + lane];
+    for (int e = 0; e < J; ++e) ul[e] = su[e * SU + lane];
 
     // ---- the rows: codebook look-ups against the lane's transformed values
-    auto dot_row = [&](const uint32_t(&w)[NWI], unsigned short scale_h, int j) {
+    auto lane_dot = [&](const uint32_t(&w)[NWI]) {
         float acc = 0.0f;
 #pragma unroll
         for (int e = 0; e < J; ++e) {
             const uint32_t c = (w[e >> 3] >> (4 * (e & 7))) & 15u;
             acc = fmaf(scb[c], ul[e], acc);
         }
-        acc = warp_sum(acc);
+        return acc;
+    };
+    auto dot_row = [&](const uint32_t(&w)[NWI], unsigned short scale_h, int j) {
+        const float acc = warp_sum(lane_dot(w));
         if (lane == 0) p.y[j] = half_bits_to_float(scale_h) * acc;
     };
+    // the preloaded rows: the lane sums of RR of them reduced together (RR - 1 halving
+    // shuffles and log2(32 / RR) more instead of 5 per row); lane (32 / RR) i then holds
+    // row i's total
+    auto joint = [&](auto rr) {
+        constexpr int RR = decltype(rr)::value;
+        float acc[RR];
 #pragma unroll
-    for (int i = 0; i < RPW; ++i)
-        if (i < my_rows) dot_row(wi[i], sh[i], gw + i * tw);
+        for (int i = 0; i < RR; ++i) acc[i] = lane_dot(wi[i]);
+        stream::halving_reduce<RR, 5>(acc);
+        constexpr int LPR = 32 / RR;
+        const int i = lane / LPR;
+        uint32_t s_me = sh[0];
+#pragma unroll
+        for (int r = 1; r < RR; ++r) s_me = i == r ? sh[r] : s_me;
+        if (lane % LPR == 0 && i < my_rows) p.y[gw + i * tw] = half_bits_to_float((unsigned short)s_me) * acc[0];
+    };
+    static_assert(RPW == 4, "rows preloaded per warp");
+    if (my_rows >= 3)
+        joint(std::integral_constant<int, 4>{});
+    else if (my_rows == 2)
+        joint(std::integral_constant<int, 2>{});
+    else if (my_rows == 1)
+        dot_row(wi[0], sh[0], gw);
     for (int i = RPW; i < my_rows; ++i) {
         const int j = gw + i * tw;
         const int r = p.row_start + j;
@@ -268,7 +294,7 @@ __global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
 template <int J>
 static int launch_cq_onegroup_t(const CqParams& p, const LaunchCtx& lc) {
     auto kern = cq_onegroup_kernel<J>;
-    const size_t smem = (size_t)2 * 32 * J * sizeof(float);
+    const size_t smem = (size_t)(33 + 32) * J * sizeof(float);
     if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
     int grid = (p.row_count + 7) / 8;  // at least one row per warp
     if (grid > lc.sm_count * 2) grid = lc.sm_count * 2;

@@ -181,8 +181,10 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
     constexpr int PARTS = NB > SB ? NB / SB : 1;      // stages per row
     constexpr int JU = GEN ? (R * NB + 31) / 32 : JL;  // blocks per lane that can be in a stage
     // HALF (48-block rows, 10 per 512-block stage): rows 2i and 2i+1 go to the two half
-    // warps, lane l taking blocks 3 (l % 16) .. 3 (l % 16) + 2 of row 2i + l / 16 (j = 3i + q),
+    // warps, lane l taking blocks l % 16 + 16q (q = 0, 1, 2) of row 2i + l / 16 (j = 3i + q),
     // so each lane sums its own three blocks per row and a row is reduced over 16 lanes.
+    // A half warp's loads of one j are then 16 consecutive blocks: their 2-byte scales
+    // fill 8 banks, the other half's (96 bytes on) 8 others.
     // Otherwise lane l takes blocks l + 32j of the stage.
     constexpr bool HALF = GEN && R == 10;
     // distinct activation blocks per lane.  GEN (48 blocks per row): lane l meets blocks
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
         const unsigned char* st = slots + (size_t)slot_ * SL::BYTES;
 #pragma unroll
         for (int j = 0; j < JU; ++j) {
-            const int fb = HALF ? (2 * (j / 3) + (lane >> 4)) * NB + 3 * (lane & 15) + j % 3 : lane + 32 * j;
+            const int fb = HALF ? (2 * (j / 3) + (lane >> 4)) * NB + (lane & 15) + 16 * (j % 3) : lane + 32 * j;
             if constexpr (BITS == 2) {
                 cw[j] = make_uint4(0u, 0u, 0u, 0u);
                 hw[j] = *reinterpret_cast<const uint2*>(st + 8 * fb);
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
     if constexpr (XREG) {
 #pragma unroll
         for (int j = 0; j < NXR; ++j) {
-            const int blk = HALF  ? 3 * (lane & 15) + j
+            const int blk = HALF  ? (lane & 15) + 16 * j
                             : GEN ? (lane + 32 * j) % NB
                             : NB >= 32 ? lane + 32 * j
                                        : (lane & (NB - 1));
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                     pj[c][j] = combine<BITS>(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), dh[j], mh[j], xs[c][xj],
                                              xS[c][xj]);
                 } else {
-                    const int blk = HALF  ? 3 * (lane & 15) + j % 3
+                    const int blk = HALF  ? (lane & 15) + 16 * (j % 3)
                                     : GEN ? (lane + 32 * j) % NB
                                           : (part * SB + lane + 32 * j) & (NB - 1);
                     const XqView v = xq_view(xqbase + c * xstride, NB);

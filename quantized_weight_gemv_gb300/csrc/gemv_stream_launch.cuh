@@ -49,14 +49,18 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     // per warp: a slot is refilled as soon as it has been copied to registers, and the
     // stream of a large matrix keeps every warp busy (measured on GB300 as the fastest
     // shape for the vocabulary heads and the large projections).
-    // A GEMV of one or two columns whose share per SM is one to four stages per warp of
+    // A GEMV of up to four columns whose share per SM is one to four stages per warp of
     // one 16-warp CTA (for 16384 x 2048: 27 stages of 5 KB per SM) takes that CTA, with enough
     // slots that every stage of every warp is requested before the kernel waits for the
     // preceding work (one stage in registers, the rest in slots): the weight stream then
     // overlaps the preceding kernel's tail and the activation prologue.
+    // Q6 at three or four columns keeps the 8-warp form: its 16-warp kernel exceeds the
+    // 128 registers a thread has there and spills (16384 x 2048, four columns: 15.5 us
+    // against 11.7 us measured on GB300).
     // QG_STREAM_WARPS (8 or 16), QG_STREAM_SLOTS and QG_STREAM_CTAS_PER_SM override it.
+    constexpr bool W16 = BC <= 4 && EPI == EPI_STORE && !(BITS == 6 && BC == 4);
     int W = 8, D = 1, per_sm = BC <= 2 ? 2 : 1;
-    if constexpr (BC <= 4 && EPI == EPI_STORE) {
+    if constexpr (W16) {
         const long long rows = ((long long)p.n + lc.sm_count - 1) / lc.sm_count;
         const long long stages = (NB >= SB ? rows : (rows + R - 1) / R) * PARTS;
         const long long per_warp = (stages + 15) / 16;
@@ -69,7 +73,7 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     }
     D = env_int("QG_STREAM_SLOTS", D);
     per_sm = env_int("QG_STREAM_CTAS_PER_SM", per_sm);
-    if constexpr (BC <= 4 && EPI == EPI_STORE) {
+    if constexpr (W16) {
         if (W == 16) return launch_w<BITS, BC, EPI, NB, 16>(p, lc, D, per_sm);
     }
     return launch_w<BITS, BC, EPI, NB, 8>(p, lc, D, per_sm);

@@ -125,13 +125,14 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
     float* C0 = reinterpret_cast<float*>(img + Smem<NT>::C0_off(nb));
     const int nf4 = k >> 2;
     const int total = min(8 * NT * nf4, item_end);  // columns beyond the batch quantise zeros
+    const int nf4_log2 = __ffs(nf4) - 1;             // k is a power of two here (512..2048)
     constexpr int CHUNK = 8;
     for (int r0 = item0; r0 < total; r0 += nthreads * CHUNK) {
         float4 rv[CHUNK];
 #pragma unroll
         for (int i = 0; i < CHUNK; ++i) {
             const int idx_all = r0 + i * nthreads + t;
-            const int c = idx_all / nf4;
+            const int c = idx_all >> nf4_log2;
             rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (idx_all < total && c < batch)
                 rv[i] = __ldg(reinterpret_cast<const float4*>(X + (size_t)c * k) + (idx_all - c * nf4));
@@ -140,7 +141,7 @@ __device__ __forceinline__ void quantize_to_frags(const float* __restrict__ X, i
         for (int i = 0; i < CHUNK; ++i) {
             if (r0 + i * nthreads >= total) break;  // the same for every thread: nothing left in this round
             const int idx_all = r0 + i * nthreads + t;
-            const int c = idx_all / nf4;
+            const int c = idx_all >> nf4_log2;
             const int idx = idx_all - c * nf4;
             const float4 r = rv[i];
             float a = fmaxf(fmaxf(fabsf(r.x), fabsf(r.y)), fmaxf(fabsf(r.z), fabsf(r.w)));

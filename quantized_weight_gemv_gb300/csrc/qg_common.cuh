@@ -131,6 +131,8 @@ __device__ __forceinline__ void quantize_runs(const float* __restrict__ x, int k
     const int nrun = k / V;          // runs per column
     const int total = batch * nrun;
     const int m = t & (LPB - 1);     // run within the block
+    // column of run idx: idx / nrun, a shift when nrun is a power of two (k = 2^j)
+    const int nrun_log2 = (nrun & (nrun - 1)) == 0 ? __ffs(nrun) - 1 : -1;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     for (int r0 = 0; r0 < total; r0 += NT * CHUNK) {
         float4 r[CHUNK][F];
@@ -177,7 +179,7 @@ __device__ __forceinline__ void quantize_runs(const float* __restrict__ x, int k
 #pragma unroll
             for (int o = 1; o < LPB; o <<= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
             if (idx < total) {
-                const int c = batch == 1 ? 0 : idx / nrun;  // (no division for one column)
+                const int c = batch == 1 ? 0 : nrun_log2 >= 0 ? idx >> nrun_log2 : idx / nrun;
                 const int b = (idx - c * nrun) / LPB;
                 const XqView v = xq_view(base + (size_t)c * stride, nb);
                 int8_t* dst = m < LPB / 2 ? v.lo + 16 * b + V * m : v.hi + 16 * b + V * (m - LPB / 2);

@@ -87,7 +87,8 @@ def test_blockdots_extremes_bit_exact():
 
 # ---------------------------------------------------------------- GEMV
 SHAPES = [(1, 32), (7, 96), (33, 256), (100, 512), (1000, 1024), (1024, 1024), (333, 2048), (2049, 2048),
-          (77, 4096), (19, 8192), (40, 16384), (3, 1056), (5, 32768), (1, 1536), (4, 1536), (1234, 1536)]
+          (77, 4096), (19, 8192), (40, 16384), (3, 1056), (5, 32768), (1, 1536), (4, 1536), (1234, 1536),
+          (3, 65536)]  # the largest k the calls accept (QG_MAX_K)
 
 
 @pytest.mark.parametrize("bits", [2, 4, 6])

@@ -15,7 +15,9 @@
  *    caller; the library keeps no reference to them after the call returns.
  *  - Calls are asynchronous: arguments are validated on the host, the work is
  *    enqueued on `stream` (a cudaStream_t passed as void*; NULL is the legacy
- *    default stream) and the call returns without synchronising.
+ *    default stream) and the call returns without synchronising.  The stream and
+ *    every buffer belong to the current device (cudaGetDevice), whose properties
+ *    and device-side words the call uses.
  *  - A negative return value is an error; nothing was enqueued and no output
  *    was touched.  QG_ERR_CUDA reports a launch failure seen right after the
  *    launch; faults raised while a kernel runs surface at the caller's next
@@ -122,7 +124,7 @@ int qgemv_q6(const uint8_t* lo, const uint8_t* hi, const uint16_t* scale, const 
  *   bits : 2 (hi and min NULL), 4 (hi NULL) or 6
  *   1 <= batch <= QG_MAX_BATCH;  batch * k <= 131072
  *   X : device fp32 [batch][k];  Y : device fp32 [batch][n] (written)
- * For batch >= 8 with 4-bit weights and k in {512, 1024, 2048, 4096} the integer
+ * For batch >= 8 with 4-bit weights and k in {512, 1024, 2048} the integer
  * block dots run on tensor cores (mma.sync, f16 operands, exact).  That path quantises
  * the activations once into `ws` (at least qg_batched_workspace_bytes(bits, k, batch)
  * bytes of device memory, 16-byte aligned, no initial content; 0 bytes are needed for

@@ -236,12 +236,17 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
     const int half_nb = nb >> 1;
     const int TPT = half_nb / KC;                 // tiles per task: 1, 2 or 4
     const int LT = TPT == 1 ? 0 : TPT == 2 ? 1 : 2;  // log2(TPT)
-    const int n_tasks = 2 * n_groups;
-    const int wstride = gridDim.x * NW;
-    const int task0 = blockIdx.x * NW + warp;
+    // this CTA's row groups: an equal share [rg0, rg1) of all, so that every SM takes
+    // part; its tasks are the (row group, k half) pairs, warp w taking tasks w, w + NW, ...
+    // (NW even: the two halves of a row group fall to warps w and w ^ 1)
+    const int rg0 = (int)((long long)n_groups * blockIdx.x / gridDim.x);
+    const int rg1 = (int)((long long)n_groups * (blockIdx.x + 1) / gridDim.x);
+    const int n_tasks = 2 * (rg1 - rg0);
+    const int wstride = NW;
+    const int task0 = warp;
     const int my_tasks = task0 < n_tasks ? (n_tasks - task0 + wstride - 1) / wstride : 0;
     const int n_tiles = my_tasks * TPT;
-    auto tile_rg = [&](int q) { return (task0 + (q >> LT) * wstride) >> 1; };
+    auto tile_rg = [&](int q) { return rg0 + ((task0 + (q >> LT) * wstride) >> 1); };
     auto tile_blk = [&](int q) { return (warp & 1) * half_nb + (q & (TPT - 1)) * KC; };
 
     // weights do not depend on earlier work: start the first tiles before waiting for it
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(NW * 32, 1) mma_batched_kernel(PlainParams p, 
     const float* other = part + (size_t)(warp ^ 1) * 16 * 8 * NT;
     const int pair_bar = 1 + (warp >> 1);
     for (int task = 0; task < my_tasks; ++task) {
-        const int rg = (task0 + task * wstride) >> 1;
+        const int rg = rg0 + ((task0 + task * wstride) >> 1);
         float acc[NT][4];
 #pragma unroll
         for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
@@ -388,8 +393,8 @@ static int launch_mma_t(const PlainParams& p, unsigned char* ws, const LaunchCtx
     const int n_groups = (p.n + 15) >> 4;
     const size_t smem = mma::Smem<NT>::bytes(nb);
     if (smem > (size_t)lc.max_smem_optin - 1024) return QG_ERR_UNSUPPORTED;
-    int grid = (2 * n_groups + mma::NW - 1) / mma::NW;  // one (row group, k half) task per warp
-    if (grid > lc.sm_count) grid = lc.sm_count;
+    int grid = n_groups;  // at most one row group per CTA ...
+    if (grid > lc.sm_count) grid = lc.sm_count;  // ... and one CTA per SM, every SM taking part
     if (grid < 1) grid = 1;
     if (!ws) {
         auto kern = mma::mma_batched_kernel<NT, false>;

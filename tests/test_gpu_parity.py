@@ -378,6 +378,26 @@ def test_batched_tensor_core_with_and_without_workspace(batch, k):
             assert_close(Y[b], refs[b])
 
 
+@pytest.mark.parametrize("batch", [8, 11, 16])
+@pytest.mark.parametrize("k", [512, 1024, 2048])
+def test_batched_tensor_core_launch_forms_identical(batch, k):
+    """The tensor-core path's two forms make the same activation image, so the same bits:
+    the image quantised once into a workspace (two launches) and every CTA quantising
+    alone (no workspace); both against the oracle too.  Row counts below and above the
+    grid, one ragged row group."""
+    for n in (50, 16384 + 9):
+        w = datagen.make_quantized(4, 2600 + k + batch + n, n, k)
+        X = datagen.normal_f32(2600 + k + batch + n, 1, batch * k).reshape(batch, k)
+        wd = dev_w(w)
+        Xt = torch.from_numpy(X).to(DEV)
+        Ya = qg.qgemv_batched(4, wd["lo"], None, wd["scale"], wd["min"], Xt, ws="auto").cpu().numpy()
+        Yn = qg.qgemv_batched(4, wd["lo"], None, wd["scale"], wd["min"], Xt, ws=None).cpu().numpy()
+        assert np.array_equal(Ya, Yn)
+        for b in (0, batch // 2, batch - 1):
+            assert_close(Ya[b], oracle_gemv_par(w, X[b]) if n > 1000 else oracle.gemv(w, X[b]))
+    assert qg.device_error() == 0
+
+
 @pytest.mark.parametrize("batch", [8, 12, 16])
 @pytest.mark.parametrize("k", [512, 2048])
 def test_batched_tensor_core_block_dot_exact(batch, k):

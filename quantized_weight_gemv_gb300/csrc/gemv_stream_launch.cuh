@@ -57,12 +57,17 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     // Q6 at three or four columns keeps the 8-warp form: its 16-warp kernel exceeds the
     // 128 registers a thread has there and spills (16384 x 2048, four columns: 15.5 us
     // against 11.7 us measured on GB300).
+    // A smaller GEMV (fewer than 16 stages per SM: 1024 x 1024, 2048 x 2048) takes one
+    // 8-warp CTA per SM: a second CTA per SM adds no stream there, only launch and
+    // completion work (1024 x 1024 2.06 -> 1.77 us, 2048 x 2048 2.38 -> 2.09 us back to back
+    // on GB300).
     // QG_STREAM_WARPS (8 or 16), QG_STREAM_SLOTS and QG_STREAM_CTAS_PER_SM override it.
     constexpr bool W16 = BC <= 4 && EPI == EPI_STORE && !(BITS == 6 && BC == 4);
     int W = 8, D = 1, per_sm = BC <= 2 ? 2 : 1;
+    const long long rows = ((long long)p.n + lc.sm_count - 1) / lc.sm_count;
+    const long long stages = (NB >= SB ? rows : (rows + R - 1) / R) * PARTS;  // per SM
+    if (stages < 16) per_sm = 1;
     if constexpr (W16) {
-        const long long rows = ((long long)p.n + lc.sm_count - 1) / lc.sm_count;
-        const long long stages = (NB >= SB ? rows : (rows + R - 1) / R) * PARTS;
         const long long per_warp = (stages + 15) / 16;
         if (stages >= 16 && per_warp <= 4) {
             W = 16;

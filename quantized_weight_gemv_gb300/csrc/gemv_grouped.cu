@@ -502,8 +502,8 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
     // and one ring slot per warp - measured on GB300 as the fastest shape: the slot is
     // refilled as soon as it has been copied to registers, so 16 x 5 KB stay in flight
     // per SM.  The diagnostic switches QG_GROUPED_CTAS_PER_SM (1 or 2: the kernel's
-    // register bound), QG_GROUPED_GRID_PER_SM (1 or 2: the grid, by default the same) and
-    // QG_GROUPED_SLOTS (slots per warp) override it.
+    // register bound), QG_GROUPED_GRID_PER_SM (1 or 2: the grid, by default the same
+    // except for short groups, below) and QG_GROUPED_SLOTS (slots per warp) override it.
     int per_sm = env_int("QG_GROUPED_CTAS_PER_SM", 2);
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 2) per_sm = 2;
@@ -523,7 +523,10 @@ int launch_grouped(int bits, const qg_gemv_desc* descs, int count, unsigned char
          {grouped_gemv_kernel<6, 2, false>, grouped_gemv_kernel<6, 2, true>}}};
     const K kern = kerns[bits == 4 ? 0 : 1][per_sm - 1][smx ? 1 : 0];
     if (int e = ensure_smem_attr((const void*)kern, smem, lc)) return e;
-    int grid_per_sm = env_int("QG_GROUPED_GRID_PER_SM", per_sm);
+    // A short group (fewer stages than 8 per SM: the chain's q/k/v and o phases) takes one
+    // CTA per SM: a second adds no stream there, and the next launch's CTAs find room
+    // beside it while it runs (decode chain 798 -> 753 us per token on GB300).
+    int grid_per_sm = env_int("QG_GROUPED_GRID_PER_SM", stages < 8LL * lc.sm_count ? 1 : per_sm);
     if (grid_per_sm < 1) grid_per_sm = 1;
     if (grid_per_sm > 2) grid_per_sm = 2;
     long long grid = (long long)lc.sm_count * grid_per_sm;

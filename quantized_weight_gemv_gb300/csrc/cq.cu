@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
 //    __shfl_xor_sync, and the top three (the warp bits) after one pass through shared
 //    memory, where each of 4J threads takes the eight elements c + 4J*m (m < 8) of one
 //    column c.  Its results, times 1/sqrt(G), go to the dot layout (element J*l + e at
-//    e*32 + l).
+//    e*33 + l: the padded row stride keeps the scatter free of bank conflicts).
 //  * Each lane then holds its J transformed values in registers for all its rows: per
 //    row only the codebook look-ups (16 entries in 16 distinct banks: conflict-free for
 //    any index pattern) and the fused multiply-adds remain.
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
                 }
             }
         }
-        // element i = t + 4J*m goes to (i % J) * 32 + i / J
+        // element i = t + 4J*m goes to (i % J) * SU + i / J
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int i = t + 4 * J * m;

@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
     // fill 8 banks, the other half's (96 bytes on) 8 others.
     // Otherwise lane l takes blocks l + 32j of the stage.
     constexpr bool HALF = GEN && R == 10;
-    // distinct activation blocks per lane.  GEN (48 blocks per row): lane l meets blocks
-    // (l + 32j) mod 48, and 96 = 0 mod 48, so only the three of j mod 3
+    // distinct activation blocks per lane.  GEN (48 blocks per row): three, l % 16 + 16q
+    // under HALF, else (l + 32j) mod 48, where 96 = 0 mod 48 leaves only j mod 3
     constexpr int NXB = GEN ? 3 : NB >= 32 ? (NB < SB ? NB / 32 : JL) : 1;
     // activation words in registers, except for four columns of rows of 64+ blocks, whose
     // 80 registers of words would leave room for only one 8-warp CTA per SM

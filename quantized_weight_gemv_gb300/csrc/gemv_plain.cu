@@ -77,8 +77,7 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(PlainParams p) {
     }
     if constexpr (EPI == EPI_ARGMAX) {
         __shared__ ArgmaxPartial sred[8];
-        __shared__ int sflag;
-        argmax_finish(bv, bi, p.ws, p.argmax, sred, &sflag);
+        argmax_finish(bv, bi, p.ws, p.argmax, sred);
     }
 }
 
@@ -138,7 +137,7 @@ static int launch_plain_t(const PlainParams& p, const LaunchCtx& lc) {
     if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
     int rows_ctas = (p.n + 7) / 8;
     int grid = lc.sm_count * 8;
-    if (EPI == EPI_ARGMAX) grid = lc.sm_count * 4 < VOCAB_MAX_CTAS ? lc.sm_count * 4 : VOCAB_MAX_CTAS;
+    if (EPI == EPI_ARGMAX) grid = lc.sm_count * 4;
     if (grid > rows_ctas) grid = rows_ctas;
     if (grid < 1) grid = 1;
     return launch_kernel(kern, dim3(grid), dim3(256), smem, lc, p);

@@ -145,16 +145,29 @@ __host__ __device__ constexpr size_t xq_offset(int nslots, int slot_bytes) {
     return (((size_t)nslots * (size_t)(slot_bytes + 8)) + 15) & ~(size_t)15;
 }
 
+// One finished row: stored (EPI_STORE), or soft-capped, stored when logits are wanted and
+// folded into the lane's running (value, index) best; under EPI_SELECT also into its
+// online log-sum-exp (lm, ls; NaN skipped), the best only when no allowed list restricts it.
 template <int EPI, int BC>
 __device__ __forceinline__ void emit_row(const StreamParams& p, long long row, const float (&v)[BC], float& bv,
-                                         int& bi, float inv_c) {
+                                         int& bi, float& lm, float& ls, float inv_c) {
     if constexpr (EPI == EPI_STORE) {
+        (void)lm;
+        (void)ls;
 #pragma unroll
         for (int c = 0; c < BC; ++c)
             if (c < p.batch) p.y[(size_t)c * p.n + row] = v[c];
     } else if constexpr (EPI == EPI_SELECT) {
-        p.y[row] = softcap_apply(v[0], p.softcap, inv_c);  // folded into the selection at the CTA's end
+        const float l = softcap_apply(v[0], p.softcap, inv_c);
+        p.y[row] = l;
+        if (l == l) lse_merge(lm, ls, l, 1.0f);
+        if (!p.allowed && better(l, (int)row, bv, bi)) {
+            bv = l;
+            bi = (int)row;
+        }
     } else {
+        (void)lm;
+        (void)ls;
         const float l = softcap_apply(v[0], p.softcap, inv_c);
         if (p.y) p.y[row] = l;
         if (better(l, (int)row, bv, bi)) {
@@ -194,6 +207,9 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
     // 80 registers of words would leave room for only one 8-warp CTA per SM
     constexpr bool XREG = NB <= 128 && BC * NXB <= (BC == 4 ? 4 : 8);
     constexpr int NXR = XREG ? NXB : 1;
+    // Q2 in the HALF mapping with the activation words in registers: a lane's three blocks
+    // of a row meet its three activation blocks, so their scales multiply in the row sum
+    constexpr bool SFOLD = BITS == 2 && HALF && XREG;
     static_assert(!GEN || NB == 48, "blocks per row: a power of two, or 48");
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -283,6 +299,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
 
     uint4 xl[BC][NXR], xh[BC][NXR];
     float xs[BC][NXR], xS[BC][NXR];
+    int xT[BC][NXR];  // Q2: 64 x the zero-point term -2 S_b, the seed of the block dot
     if constexpr (XREG) {
 #pragma unroll
         for (int j = 0; j < NXR; ++j) {
@@ -298,12 +315,14 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                 xh[c][j] = ok ? *reinterpret_cast<const uint4*>(v.hi + 16 * blk) : make_uint4(0, 0, 0, 0);
                 xs[c][j] = ok ? v.s[blk] : 0.0f;
                 xS[c][j] = ok ? v.S[blk] : 0.0f;
+                xT[c][j] = -128 * __float2int_rn(xS[c][j]);
             }
         }
     }
 
     float bv = __int_as_float(0x7fc00000);
     int bi = 0x7fffffff;
+    float lm = -INFINITY, ls = 0.0f;  // selection: online log-sum-exp of the emitted logits
     const float inv_c = softcap_inv(p.softcap);
     float rowacc[BC];  // running sum of a row that spans several stages
 #pragma unroll
@@ -331,7 +350,14 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
         for (int j = 0; j < JU; ++j) {
 #pragma unroll
             for (int c = 0; c < BC; ++c) {
-                if constexpr (XREG) {
+                if constexpr (XREG && BITS == 2) {
+                    // scale * (D - 2 S_b) straight from the seeded dot; the activation scale
+                    // s_b is applied in the row sums under SFOLD, else here
+                    const int xj = NB >= 32 ? (j % NXR) : 0;
+                    const float t = half_bits_to_float(dh[j]) *
+                                    (float)block_dot_q2(hw[j], xl[c][xj], xh[c][xj], xT[c][xj]);
+                    pj[c][j] = SFOLD ? t : xs[c][xj] * t;
+                } else if constexpr (XREG) {
                     const int xj = NB >= 32 ? (j % NXR) : 0;
                     pj[c][j] = combine<BITS>(qdot<BITS>(cw[j], hw[j], xl[c][xj], xh[c][xj]), dh[j], mh[j], xs[c][xj],
                                              xS[c][xj]);
@@ -357,7 +383,11 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int j = i < 5 ? 3 * i : 0;  // JU = 15: j + 2 < JU for every row pair
-                    rs[i] = i < 5 ? pj[c][j] + pj[c][j + 1] + pj[c][j + 2] : 0.0f;
+                    if constexpr (SFOLD)  // block j + q meets activation block q of the lane
+                        rs[i] = i < 5 ? fmaf(xs[c][2], pj[c][j + 2], fmaf(xs[c][1], pj[c][j + 1], xs[c][0] * pj[c][j]))
+                                      : 0.0f;
+                    else
+                        rs[i] = i < 5 ? pj[c][j] + pj[c][j + 1] + pj[c][j + 2] : 0.0f;
                 }
                 halving_reduce<8, 4>(rs);
                 pj[c][0] = rs[0];
@@ -367,7 +397,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                 float out[BC];
 #pragma unroll
                 for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
+                emit_row<EPI, BC>(p, row0 + r, out, bv, bi, lm, ls, inv_c);
             }
         } else if constexpr (GEN) {
             // rows straddle the lanes' block groups: block l + 32j of lane l lies in row
@@ -398,7 +428,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                     float out[BC];
 #pragma unroll
                     for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
+                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi, lm, ls, inv_c);
                 }
             }
         } else if constexpr (NB >= 32) {
@@ -435,7 +465,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                         float out[BC];
 #pragma unroll
                         for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                        emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
+                        emit_row<EPI, BC>(p, row0 + r, out, bv, bi, lm, ls, inv_c);
                     }
                 }
             }
@@ -451,7 +481,7 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
                     float out[BC];
 #pragma unroll
                     for (int c = 0; c < BC; ++c) out[c] = pj[c][0];
-                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi, inv_c);
+                    emit_row<EPI, BC>(p, row0 + r, out, bv, bi, lm, ls, inv_c);
                 }
             }
         }
@@ -459,29 +489,21 @@ __global__ void __launch_bounds__(W * 32, (W == 8 && BC <= 2) ? 2 : 1) gemv_stre
 
     if constexpr (EPI == EPI_ARGMAX) {
         __shared__ ArgmaxPartial sred[W];
-        __shared__ int sflag;
-        argmax_finish(bv, bi, p.ws, p.argmax, sred, &sflag);
+        argmax_finish(bv, bi, p.ws, p.argmax, sred);
     } else if constexpr (EPI == EPI_SELECT) {
-        // Constrained selection over this CTA's rows [r0, r1), which its warps have just
-        // written to y (visible to the whole CTA after the barrier): an online
-        // log-sum-exp (NaN skipped) and the best (value, lowest id) among the allowed ids
-        // that fall in the range, from one pass over the allowed list; the last CTA to
-        // finish merges every CTA's partial.
+        // Constrained selection over this CTA's rows [r0, r1): each lane's online
+        // log-sum-exp of the rows it emitted (NaN skipped) and, without a list, its best
+        // (value, lowest id); with a list, the best among the allowed ids that fall in the
+        // range, from one pass over the list after the barrier (the CTA's logits in y are
+        // then visible to all its threads).  The last CTA to finish merges every CTA's
+        // partial.
         __shared__ SelectPartial sred[W];
         __shared__ int slast;
-        __syncthreads();
-        float m = -INFINITY, s = 0.0f;
-        float sv = __int_as_float(0x7fc00000);
-        int si = 0x7fffffff;
-        for (long long i = r0 + threadIdx.x; i < r1; i += blockDim.x) {
-            const float l = p.y[i];
-            if (l == l) lse_merge(m, s, l, 1.0f);
-            if (!p.allowed && better(l, (int)i, sv, si)) {
-                sv = l;
-                si = (int)i;
-            }
-        }
+        float m = lm, s = ls;
+        float sv = bv;
+        int si = bi;
         if (p.allowed) {
+            __syncthreads();
             for (int j = threadIdx.x; j < p.n_allowed; j += blockDim.x) {
                 const long long id = p.allowed[j];
                 if (id < r0 || id >= r1) continue;

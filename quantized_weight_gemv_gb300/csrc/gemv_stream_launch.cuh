@@ -33,7 +33,6 @@ int launch_w(StreamParams p, const LaunchCtx& lc, int D, int per_sm) {
     p.err = lc.err;
     if (per_sm < 1) per_sm = 1;
     int grid = lc.sm_count * per_sm;
-    if (EPI == EPI_ARGMAX && grid > VOCAB_MAX_CTAS) grid = VOCAB_MAX_CTAS;
     if (EPI == EPI_SELECT && grid > SELECT_MAX_CTAS) grid = SELECT_MAX_CTAS;
     if (grid > p.n) grid = p.n;
     if (grid < 1) grid = 1;
@@ -61,12 +60,16 @@ int launch_t(StreamParams p, const LaunchCtx& lc) {
     // 8-warp CTA per SM: a second CTA per SM adds no stream there, only launch and
     // completion work (1024 x 1024 2.06 -> 1.77 us, 2048 x 2048 2.38 -> 2.09 us back to back
     // on GB300).
+    // Q2 streams take two slots per warp: its 10-byte blocks are few instructions each, so a
+    // warp finishes a stage in about one DRAM round trip and a single refilled slot leaves
+    // it waiting (262144 x 1536 with soft-cap and argmax: 25.5 -> 24.4 us on GB300).
     // QG_STREAM_WARPS (8 or 16), QG_STREAM_SLOTS and QG_STREAM_CTAS_PER_SM override it.
     constexpr bool W16 = BC <= 4 && EPI == EPI_STORE && !(BITS == 6 && BC == 4);
     int W = 8, D = 1, per_sm = BC <= 2 ? 2 : 1;
     const long long rows = ((long long)p.n + lc.sm_count - 1) / lc.sm_count;
     const long long stages = (NB >= SB ? rows : (rows + R - 1) / R) * PARTS;  // per SM
     if (stages < 16) per_sm = 1;
+    if (BITS == 2 && stages >= 16) D = 2;
     if constexpr (W16) {
         const long long per_warp = (stages + 15) / 16;
         if (stages >= 16 && per_warp <= 4) {

@@ -45,7 +45,7 @@ def test_status_strings_and_version(lib):
         assert qg.status_string(code) not in ("", "unknown status")
     assert qg.status_string(-99) == "unknown status"
     assert lib.qg_version() >= 100
-    assert lib.qg_vocab_workspace_bytes() >= 256 + 8 * 152
+    assert 16 <= lib.qg_vocab_workspace_bytes() <= 4096  # a small fixed amount (counter and packed key)
 
 
 P = ctypes.c_void_p

@@ -250,6 +250,45 @@ def test_vocab_planted_maximum_and_ties(flags):
     assert _vocab_check(w, x, 30.0, flags) == 12345
 
 
+@pytest.mark.parametrize("k", [256, 1536])
+@pytest.mark.parametrize("softcap", [30.0, 0.0])
+@pytest.mark.parametrize("flags", [0, qg.QG_FLAG_PLAIN])
+def test_vocab_argmax_order_edge_cases(k, softcap, flags):
+    """The argmax order across CTAs on constructed logits (Q2, all codes 0, x = 127:
+    every row's value is -nb * 8128 * scale exactly): all logits negative with the
+    maximum tied between rows in different CTAs (the lower index wins), -0 against +0
+    (equal: the lower index wins, whichever sign it has), every logit NaN (index 0),
+    and NaN everywhere but one row."""
+    n = 5000
+    q = np.zeros((n, k), np.uint8)
+    x = np.full(k, 127.0, np.float32)
+    base = np.full(n, 2.0 ** -13)
+    cases = []
+    a = base.copy()
+    a[[17, 4321]] = 2.0 ** -14
+    cases.append((a, 17))
+    for s2, s4000 in ((0.0, -0.0), (-0.0, 0.0)):
+        a = base.copy()
+        a[2], a[4000] = s2, s4000
+        cases.append((a, 2))
+    cases.append((np.full(n, np.nan), 0))
+    a = np.full(n, np.nan)
+    a[3333] = 2.0 ** -13
+    cases.append((a, 3333))
+    a = base.copy()
+    a[0] = np.nan
+    a[1] = 2.0 ** -14
+    cases.append((a, 1))
+    ws = qg.vocab_workspace(DEV)
+    for scale, want in cases:
+        w = make_w(2, q, np.repeat(scale[:, None], k // 32, axis=1), None)
+        wd = dev_w(w)
+        xt = torch.from_numpy(x).to(DEV)
+        logits, am = qg.vocab_softcap_argmax(2, wd["lo"], None, wd["scale"], None, xt, softcap, ws=ws, flags=flags)
+        l = logits.cpu().numpy()
+        assert int(am.item()) == want == oracle.argmax(l), (want, int(am.item()))
+
+
 def test_vocab_softcap_off_and_workspace_reuse():
     n, k = 4096, 2048
     w = datagen.make_quantized(6, 21, n, k)
@@ -630,6 +669,45 @@ def test_int2_vocab_head_pages_shape():
     w = datagen.make_quantized(2, 97, n, k)
     x = datagen.normal_f32(97, 1, k)
     _vocab_check(w, x, 30.0)
+
+
+@pytest.mark.parametrize("k", [1536, 2048, 512])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4])
+def test_q2_gemv_integer_exact(k, batch):
+    """Q2 (zero point 2) with the zero-point term inside the integer dot: with weight
+    scales 1 on three blocks of every row (0, 17 and the last: lanes of both half warps
+    and all three of a lane's blocks at k = 1536), 0 elsewhere, and integer activations
+    whose blocks all reach 127 (s = 1, xq = x), every output is the exact integer
+    sum over those blocks of (code - 2) * x, the oracle's fp64 value, compared bit for
+    bit.  Rows 0-3 reach the extremes (all codes 3 or 0, halves split)."""
+    n, nb = 150, k // 32
+    rng = np.random.default_rng(7100 + k + batch)
+    q = rng.integers(0, 4, (n, k)).astype(np.uint8)
+    q[0], q[1] = 3, 0
+    q[2, ::2], q[3, 1::2] = 3, 0
+    live = [0, 17 % nb, nb - 1]
+    scale = np.zeros((n, nb))
+    scale[:, live] = 1.0
+    w = make_w(2, q, scale, None)
+    X = rng.integers(-127, 128, (batch, k)).astype(np.float32)
+    X[:, ::32] = 127.0
+    X[0, :] = 127.0
+    if batch > 1:
+        X[1, :] = -127.0
+        X[1, ::32] = 127.0
+    wd = dev_w(w)
+    Xt = torch.from_numpy(X).to(DEV)
+    cols = np.concatenate([np.arange(32 * b, 32 * b + 32) for b in sorted(set(live))])
+    for b in range(batch):  # the reference is the integer sum itself
+        ref = oracle.gemv(w, X[b])
+        want = (q[:, cols].astype(np.int64) - 2) @ X[b, cols].astype(np.int64)
+        assert np.array_equal(ref, want.astype(np.float64))
+    for ws in ("auto", None):
+        Y = qg.qgemv_batched(2, wd["lo"], None, wd["scale"], None, Xt, ws=ws).cpu().numpy()
+        for b in range(batch):
+            assert np.array_equal(Y[b].astype(np.float64), oracle.gemv(w, X[b])), (ws, b)
+    y = gpu_gemv(wd, X[0])
+    assert np.array_equal(y, oracle.gemv(w, X[0]))
 
 
 def test_logits_select_infinities():

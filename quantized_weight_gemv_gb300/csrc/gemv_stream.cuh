@@ -28,8 +28,10 @@
 //    activation words live in registers; for long rows they are read from shared
 //    memory, stored as split halves so that the 128-bit reads are conflict-free.
 //  * Epilogues: plain store; soft-cap + argmax; soft-cap + constrained selection (each
-//    CTA folds its own rows into a log-sum-exp and an allowed best once they are
-//    written).  Both reductions end in a last-arriver merge, no CTA waits on another.
+//    lane folds the rows it emits into a log-sum-exp; the allowed best is taken from
+//    the CTA's written rows).  Both reductions end with the last CTA to arrive at a
+//    counter finishing the result (the argmax from one packed atomic key, the selection
+//    from every CTA's partial); no CTA waits on another.
 //  * Every wait is bounded (mbarrier try_wait against %globaltimer); on expiry the
 //    kernel ORs a code into the library's device error word and stops.
 #pragma once

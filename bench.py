@@ -76,6 +76,7 @@ CASES = {
     "q4_batched_b8_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
     "cq_8192x512": None,  # the CQ matvec, 64 rotating copies (run_cq_case)
+    "cq_8192x2048_g512": None,  # the CQ matvec with four groups per row (cq_kernel), 24 rotating copies
     "read_floor_20971520B": None,  # the plain-read floor hook over 8 rotating 21 MB buffers (run_floor_case)
     "select_262144": None,  # constrained selection over 262144 logits, 1 % allowed (run_select_case)
     "q4_chain_persistent": None,  # the decode chain, --layers layers (run_chain_case)
@@ -134,27 +135,37 @@ def run_stream_case(args):
 
 
 def run_cq_case(args):
-    """Profiling case: the 8192 x 512 CQ matvec over 64 rotating copies (> L2), --reps rounds."""
+    """Profiling case: the 8192 x 512 CQ matvec over 64 rotating copies (> L2), or 8192 x 2048
+    in groups of 512 (four per row) over 24, --reps rounds."""
     import torch
 
+    import datagen
     import quantized_weight_gemv_gb300 as qg
     from datagen import workloads as W
 
     device = torch.device("cuda", 0)
-    m = qg.to_device(W.cq_matrix(0), device)
-    rot = [m] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in m.items()} for _ in range(63)]
-    xc = torch.from_numpy(W.cq_x()).to(device)
-    yc = torch.empty(W.CQ_ROWS[0], device=device)
+    if args.case == "cq_8192x2048_g512":
+        n, k, copies = 8192, 2048, 24
+        m = qg.to_device(datagen.make_cq(12, n, k), device)
+        x = datagen.normal_f32(12, 1, k)
+    else:
+        n, k, copies = W.CQ_ROWS[0], W.CQ_K, 64
+        m = qg.to_device(W.cq_matrix(0), device)
+        x = W.cq_x()
+    rot = [m] + [{kk: (v.clone() if isinstance(v, torch.Tensor) else v) for kk, v in m.items()}
+                 for _ in range(copies - 1)]
+    xc = torch.from_numpy(x).to(device)
+    yc = torch.empty(n, device=device)
     state = {"i": 0}
 
     def call():
-        r = rot[state["i"] % 64]
+        r = rot[state["i"] % copies]
         state["i"] += 1
         qg.cq_fwht_matvec(r["idx"], r["codebook"], r["row_scale"], xc, W.CQ_GROUP, y=yc, flags=qg.QG_FLAG_PDL)
 
-    ms = time_eager(call, torch.cuda.current_stream(device), args.reps * 64)
-    nbytes = W.cq_bytes(W.CQ_ROWS[0], W.CQ_K)
-    print(json.dumps({"case": args.case, "calls": args.reps * 64, "us_per_call_eager": ms * 1e3,
+    ms = time_eager(call, torch.cuda.current_stream(device), args.reps * copies)
+    nbytes = W.cq_bytes(n, k)
+    print(json.dumps({"case": args.case, "calls": args.reps * copies, "us_per_call_eager": ms * 1e3,
                       "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
 
 
@@ -208,7 +219,7 @@ def run_case(args):
         return run_chain_case(args)
     if args.case == "q4_decode_stream":
         return run_stream_case(args)
-    if args.case == "cq_8192x512":
+    if args.case in ("cq_8192x512", "cq_8192x2048_g512"):
         return run_cq_case(args)
     if args.case == "select_262144":
         return run_select_case(args)

@@ -76,7 +76,7 @@ CASES = {
     "q4_batched_b8_16384x2048": (4, 16384, 2048, 8),
     "q4_batched_b16_16384x2048": (4, 16384, 2048, 8),
     "cq_8192x512": None,  # the CQ matvec, 64 rotating copies (run_cq_case)
-    "cq_8192x2048_g512": None,  # the CQ matvec with four groups per row (cq_kernel), 24 rotating copies
+    "cq_8192x2048_g512": None,  # the CQ matvec with four groups per row, 24 rotating copies
     "read_floor_20971520B": None,  # the plain-read floor hook over 8 rotating 21 MB buffers (run_floor_case)
     "select_262144": None,  # constrained selection over 262144 logits, 1 % allowed (run_select_case)
     "q4_chain_persistent": None,  # the decode chain, --layers layers (run_chain_case)
@@ -163,8 +163,15 @@ def run_cq_case(args):
         state["i"] += 1
         qg.cq_fwht_matvec(r["idx"], r["codebook"], r["row_scale"], xc, W.CQ_GROUP, y=yc, flags=qg.QG_FLAG_PDL)
 
-    ms = time_eager(call, torch.cuda.current_stream(device), args.reps * copies)
     nbytes = W.cq_bytes(n, k)
+    if args.graph:  # one round over the copies captured in a graph (PDL), replayed --reps times
+        st = torch.cuda.Stream(device)
+        g = graph_of(lambda: [call() for _ in range(copies)], st)
+        ms = time_graph(g, st, args.reps, repeats=5) / copies
+        print(json.dumps({"case": args.case, "calls": args.reps * copies, "us_per_call_graph": ms * 1e3,
+                          "GBps_graph": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
+        return
+    ms = time_eager(call, torch.cuda.current_stream(device), args.reps * copies)
     print(json.dumps({"case": args.case, "calls": args.reps * copies, "us_per_call_eager": ms * 1e3,
                       "GBps_eager": nbytes / ms / 1e6, "bytes_per_call": nbytes}), flush=True)
 

@@ -6,14 +6,17 @@
 // transform of the weights is never materialised.  "TypeGPU": one 32-lane group
 // per output row.  "Custom backend": an optional contiguous row range.
 //
-// Each warp first pulls the packed indices of its first row into L1 and loads that
-// row's scale (weights: under programmatic dependent launch they are read before the
-// preceding kernel has finished), so that their latency overlaps the transform.  Each
-// CTA transforms x itself: a warp owns a group of G = 32*J values, lane l holding
-// elements J*l .. J*l+J-1.  The butterflies over the low log2(J) index
-// bits run in registers, those over the lane bits through __shfl_xor_sync.  The
-// result is kept in shared memory transposed (element J*l + j at j*32 + l), so
-// that in the dot loop lane l reads its J values without bank conflicts.
+// Two kernels.  cq_regs_kernel (rows of up to 64 values per lane: k <= 2048, groups of
+// 256 to 1024) keeps each lane's transformed values in registers for all its rows; it
+// is described above its definition.  cq_kernel takes every other shape: each warp
+// first pulls the packed indices of its first row into L1 and loads that row's scale
+// (weights: under programmatic dependent launch they are read before the preceding
+// kernel has finished), so that their latency overlaps the transform.  Each CTA
+// transforms x itself: a warp owns a group of G = 32*J values, lane l holding elements
+// J*l .. J*l+J-1.  The butterflies over the low log2(J) index bits run in registers,
+// those over the lane bits through __shfl_xor_sync.  The result is kept in shared
+// memory transposed (element J*l + j at j*32 + l), so that in the dot loop lane l
+// reads its J values without bank conflicts.
 #include <type_traits>
 
 #include "gemv_stream.cuh"  // stream::halving_reduce
@@ -128,48 +131,66 @@ __global__ void __launch_bounds__(256) cq_kernel(CqParams p) {
     }
 }
 
-// One group per row (k == group, G = 32*J, J >= 8): the transform is split over all
-// eight warps and each warp keeps several rows in flight.
+// Up to GM groups per row (k = ng * G, ng <= GM, G = 32*J, J >= 8, GM * J <= 64): the
+// transform is split over all eight warps and each warp keeps several rows in flight.
 //  * Before griddepcontrol.wait each warp loads the packed indices of up to RPW of its
-//    rows into registers (lane l: the J/2 bytes of elements J*l .. J*l+J-1) and their
-//    scales: under programmatic dependent launch the weight reads overlap the preceding
-//    kernel's tail.
-//  * Transform: thread t holds elements E*t .. E*t+E-1 (E = J/8).  The butterflies over
-//    the low log2(E) index bits run in registers, the next five (the lane bits) through
-//    __shfl_xor_sync, and the top three (the warp bits) after one pass through shared
-//    memory, where each of 4J threads takes the eight elements c + 4J*m (m < 8) of one
-//    column c.  Its results, times 1/sqrt(G), go to the dot layout (element J*l + e at
-//    e*33 + l: the padded row stride keeps the scatter free of bank conflicts).
-//  * Each lane then holds its J transformed values in registers for all its rows: per
+//    rows into registers (lane l, group g: the J/2 bytes of the group's elements
+//    J*l .. J*l+J-1) and their scales: under programmatic dependent launch the weight
+//    reads overlap the preceding kernel's tail.
+//  * Transform, every group at once: thread t holds elements E*t .. E*t+E-1 of each group
+//    (E = J/8).  The butterflies over the low log2(E) index bits run in registers, the
+//    next five (the lane bits) through __shfl_xor_sync, and the top three (the warp bits)
+//    after one pass through shared memory, where each of 4J threads takes the eight
+//    elements c + 4J*m (m < 8) of column c of every group.  Its results, times 1/sqrt(G),
+//    go to the dot layout (element J*l + e of group g at (g*J + e)*33 + l: the padded row
+//    stride keeps the scatter free of bank conflicts).
+//  * Each lane then holds its ng*J transformed values in registers for all its rows: per
 //    row only the codebook look-ups (16 entries in 16 distinct banks: conflict-free for
 //    any index pattern) and the fused multiply-adds remain.
-template <int J>
-__global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
+template <int J, int GM>
+__global__ void __launch_bounds__(256) cq_regs_kernel(CqParams p) {
     constexpr int E = J / 8;
-    constexpr int RPW = 4;                 // rows per warp loaded before the wait
-    constexpr int NWI = (J + 7) / 8;       // index words per lane and row
+    constexpr int RPW = GM * J <= 32 ? 4 : 2;  // rows per warp loaded before the wait
+    constexpr int NWI = (J + 7) / 8;           // index words per lane, row and group
+    constexpr int NW = GM * NWI;               // index words per lane and row
+    constexpr int G = 32 * J;
     static_assert(J >= 8, "at least one element per thread");
+    static_assert(GM * J <= 64, "transformed values per lane held in registers");
     extern __shared__ __align__(16) float sm[];
     constexpr int SU = 33;  // row stride of the dot layout (32 + 1: conflict-free scatter)
-    float* su = sm;           // [J][SU], dot layout
-    float* sc = sm + J * SU;  // [32 J], natural order (transform scratch)
+    float* su = sm;                // [GM J][SU], dot layout
+    float* sc = sm + GM * J * SU;  // [GM][32 J], natural order (transform scratch)
     __shared__ float scb[16];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int tw = gridDim.x * 8;
     const int gw = blockIdx.x * 8 + wid;
     const int my_rows = p.row_count > gw ? (p.row_count - gw + tw - 1) / tw : 0;
+    const int ng = GM == 1 ? 1 : p.k / G;  // groups per row
     const size_t row_bytes = (size_t)(p.k >> 1);
+    auto has = [&](int g) { return GM == 1 || g < ng; };
 
-    uint32_t wi[RPW][NWI];
+    auto load_row = [&](int r, uint32_t(&w)[NW]) {
+        const uint8_t* rp = p.idx + (size_t)r * row_bytes + (J / 2) * lane;
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            uint32_t t[NWI];
+#pragma unroll
+            for (int q = 0; q < NWI; ++q) t[q] = 0u;
+            if (has(g)) load_lane_indices<J>(rp + (size_t)g * (G / 2), t);
+#pragma unroll
+            for (int q = 0; q < NWI; ++q) w[g * NWI + q] = t[q];
+        }
+    };
+    uint32_t wi[RPW][NW];
     unsigned short sh[RPW];
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
         sh[i] = 0;
 #pragma unroll
-        for (int q = 0; q < NWI; ++q) wi[i][q] = 0u;
+        for (int q = 0; q < NW; ++q) wi[i][q] = 0u;
         if (i < my_rows) {
             const int r = p.row_start + gw + i * tw;
-            load_lane_indices<J>(p.idx + (size_t)r * row_bytes + (J / 2) * lane, wi[i]);
+            load_row(r, wi[i]);
             sh[i] = p.row_scale[r];
         }
     }
@@ -180,28 +201,35 @@ __global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
 
     // ---- transform: registers, lanes, then warps through shared memory
     const int t = threadIdx.x;
-    float v[E];
-    if constexpr (E == 1) {
-        v[0] = p.x[t];
-    } else if constexpr (E == 2) {
-        const float2 a = reinterpret_cast<const float2*>(p.x)[t];
-        v[0] = a.x;
-        v[1] = a.y;
-    } else {
-        const float4 a = reinterpret_cast<const float4*>(p.x)[t];
-        v[0] = a.x;
-        v[1] = a.y;
-        v[2] = a.z;
-        v[3] = a.w;
+    float v[GM][E];
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+        const float* xg = p.x + (size_t)(has(g) ? g : 0) * G;
+        if constexpr (E == 1) {
+            v[g][0] = xg[t];
+        } else if constexpr (E == 2) {
+            const float2 a = reinterpret_cast<const float2*>(xg)[t];
+            v[g][0] = a.x;
+            v[g][1] = a.y;
+        } else {
+            const float4 a = reinterpret_cast<const float4*>(xg)[t];
+            v[g][0] = a.x;
+            v[g][1] = a.y;
+            v[g][2] = a.z;
+            v[g][3] = a.w;
+        }
     }
 #pragma unroll
-    for (int h = 1; h < E; h <<= 1) {
+    for (int g = 0; g < GM; ++g) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            if ((e & h) == 0) {
-                const float a = v[e], b = v[e + h];
-                v[e] = a + b;
-                v[e + h] = a - b;
+        for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                if ((e & h) == 0) {
+                    const float a = v[g][e], b = v[g][e + h];
+                    v[g][e] = a + b;
+                    v[g][e + h] = a - b;
+                }
             }
         }
     }
@@ -209,53 +237,65 @@ __global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
     for (int m = 1; m < 32; m <<= 1) {
         const bool upper = (lane & m) != 0;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
-            v[e] = upper ? (o - v[e]) : (v[e] + o);
-        }
-    }
+        for (int g = 0; g < GM; ++g) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) sc[E * t + e] = v[e];
-    __syncthreads();
-    if (t < 4 * J) {
-        float u[8];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) u[m] = sc[t + 4 * J * m];
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                if ((m & h) == 0) {
-                    const float a = u[m], b = u[m + h];
-                    u[m] = a + b;
-                    u[m + h] = a - b;
-                }
+            for (int e = 0; e < E; ++e) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[g][e], m);
+                v[g][e] = upper ? (o - v[g][e]) : (v[g][e] + o);
             }
         }
-        // element i = t + 4J*m goes to (i % J) * SU + i / J
+    }
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int i = t + 4 * J * m;
-            su[(i % J) * SU + i / J] = u[m] * p.inv_sqrt_group;
+    for (int g = 0; g < GM; ++g)
+#pragma unroll
+        for (int e = 0; e < E; ++e) sc[g * G + E * t + e] = v[g][e];
+    __syncthreads();
+    if (t < 4 * J) {
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            float u[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) u[m] = sc[g * G + t + 4 * J * m];
+#pragma unroll
+            for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    if ((m & h) == 0) {
+                        const float a = u[m], b = u[m + h];
+                        u[m] = a + b;
+                        u[m + h] = a - b;
+                    }
+                }
+            }
+            // element i = t + 4J*m of group g goes to (g*J + i % J) * SU + i / J
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int i = t + 4 * J * m;
+                su[(g * J + i % J) * SU + i / J] = u[m] * p.inv_sqrt_group;
+            }
         }
     }
     __syncthreads();
 
-    float ul[J];
+    float ul[GM * J];
 #pragma unroll
-    for (int e = 0; e < J; ++e) ul[e] = su[e * SU + lane];
+    for (int e = 0; e < GM * J; ++e) ul[e] = su[e * SU + lane];
 
     // ---- the rows: codebook look-ups against the lane's transformed values
-    auto lane_dot = [&](const uint32_t(&w)[NWI]) {
+    auto lane_dot = [&](const uint32_t(&w)[NW]) {
         float acc = 0.0f;
 #pragma unroll
-        for (int e = 0; e < J; ++e) {
-            const uint32_t c = (w[e >> 3] >> (4 * (e & 7))) & 15u;
-            acc = fmaf(scb[c], ul[e], acc);
+        for (int g = 0; g < GM; ++g) {
+            if (!has(g)) continue;
+#pragma unroll
+            for (int e = 0; e < J; ++e) {
+                const uint32_t c = (w[g * NWI + (e >> 3)] >> (4 * (e & 7))) & 15u;
+                acc = fmaf(scb[c], ul[g * J + e], acc);
+            }
         }
         return acc;
     };
-    auto dot_row = [&](const uint32_t(&w)[NWI], unsigned short scale_h, int j) {
+    auto dot_row = [&](const uint32_t(&w)[NW], unsigned short scale_h, int j) {
         const float acc = warp_sum(lane_dot(w));
         if (lane == 0) p.y[j] = half_bits_to_float(scale_h) * acc;
     };
@@ -275,26 +315,33 @@ __global__ void __launch_bounds__(256) cq_onegroup_kernel(CqParams p) {
         for (int r = 1; r < RR; ++r) s_me = i == r ? sh[r] : s_me;
         if (lane % LPR == 0 && i < my_rows) p.y[gw + i * tw] = half_bits_to_float((unsigned short)s_me) * acc[0];
     };
-    static_assert(RPW == 4, "rows preloaded per warp");
-    if (my_rows >= 3)
-        joint(std::integral_constant<int, 4>{});
-    else if (my_rows == 2)
-        joint(std::integral_constant<int, 2>{});
-    else if (my_rows == 1)
-        dot_row(wi[0], sh[0], gw);
+    static_assert(RPW == 4 || RPW == 2, "rows preloaded per warp");
+    if constexpr (RPW == 4) {
+        if (my_rows >= 3)
+            joint(std::integral_constant<int, 4>{});
+        else if (my_rows == 2)
+            joint(std::integral_constant<int, 2>{});
+        else if (my_rows == 1)
+            dot_row(wi[0], sh[0], gw);
+    } else {
+        if (my_rows >= 2)
+            joint(std::integral_constant<int, 2>{});
+        else if (my_rows == 1)
+            dot_row(wi[0], sh[0], gw);
+    }
     for (int i = RPW; i < my_rows; ++i) {
         const int j = gw + i * tw;
         const int r = p.row_start + j;
-        uint32_t w[NWI];
-        load_lane_indices<J>(p.idx + (size_t)r * row_bytes + (J / 2) * lane, w);
+        uint32_t w[NW];
+        load_row(r, w);
         dot_row(w, p.row_scale[r], j);
     }
 }
 
-template <int J>
-static int launch_cq_onegroup_t(const CqParams& p, const LaunchCtx& lc) {
-    auto kern = cq_onegroup_kernel<J>;
-    const size_t smem = (size_t)(33 + 32) * J * sizeof(float);
+template <int J, int GM>
+static int launch_cq_regs_t(const CqParams& p, const LaunchCtx& lc) {
+    auto kern = cq_regs_kernel<J, GM>;
+    const size_t smem = (size_t)(33 + 32) * GM * J * sizeof(float);
     if (int rc = ensure_smem_attr((const void*)kern, smem, lc)) return rc;
     int grid = (p.row_count + 7) / 8;  // at least one row per warp
     if (grid > lc.sm_count * 2) grid = lc.sm_count * 2;
@@ -315,15 +362,25 @@ static int launch_cq_t(const CqParams& p, const LaunchCtx& lc) {
 }
 
 int launch_cq(const CqParams& p, const LaunchCtx& lc) {
-    if (p.k == p.group) {
-        switch (p.group) {
-            case 256:
-                return launch_cq_onegroup_t<8>(p, lc);
-            case 512:
-                return launch_cq_onegroup_t<16>(p, lc);
-            case 1024:
-                return launch_cq_onegroup_t<32>(p, lc);
-        }
+    // the register form while a lane's transformed values fit (ng * J <= 64: k <= 2048),
+    // with the smallest group bound that holds the row's groups
+    const int ng = p.group > 0 ? p.k / p.group : 0;
+    switch (p.group) {
+        case 256:
+            if (ng == 1) return launch_cq_regs_t<8, 1>(p, lc);
+            if (ng == 2) return launch_cq_regs_t<8, 2>(p, lc);
+            if (ng <= 4) return launch_cq_regs_t<8, 4>(p, lc);
+            if (ng <= 8) return launch_cq_regs_t<8, 8>(p, lc);
+            break;
+        case 512:
+            if (ng == 1) return launch_cq_regs_t<16, 1>(p, lc);
+            if (ng == 2) return launch_cq_regs_t<16, 2>(p, lc);
+            if (ng <= 4) return launch_cq_regs_t<16, 4>(p, lc);
+            break;
+        case 1024:
+            if (ng == 1) return launch_cq_regs_t<32, 1>(p, lc);
+            if (ng == 2) return launch_cq_regs_t<32, 2>(p, lc);
+            break;
     }
     switch (p.group) {
         case 128:

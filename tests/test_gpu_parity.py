@@ -302,7 +302,7 @@ def test_vocab_softcap_off_and_workspace_reuse():
 
 # ---------------------------------------------------------------- CQ
 @pytest.mark.parametrize("group", [128, 256, 512, 1024])
-@pytest.mark.parametrize("n,k_groups", [(1, 1), (1024, 1), (8192, 1), (333, 2), (50, 5)])
+@pytest.mark.parametrize("n,k_groups", [(1, 1), (1024, 1), (8192, 1), (333, 2), (50, 5), (777, 3), (8192, 4), (300, 8)])
 def test_cq(group, n, k_groups):
     k = group * k_groups
     m = datagen.make_cq(4 + group, n, k)
@@ -312,21 +312,26 @@ def test_cq(group, n, k_groups):
     assert_close(y.cpu().numpy(), oracle.cq_matvec(m, x, group))
 
 
-def test_cq_row_ranges():
-    n, k = 8192, 512
+@pytest.mark.parametrize("k,group", [(512, 512), (2048, 512), (2048, 256)])
+def test_cq_row_ranges(k, group):
+    n = 8192
     m = datagen.make_cq(4, n, k)
     x = datagen.normal_f32(4, 1, k)
     md = dev_w(m)
     xt = torch.from_numpy(x).to(DEV)
-    full = oracle.cq_matvec(m, x, 512)
+    full = oracle.cq_matvec(m, x, group)
     for start, count in ((0, 1), (5, 100), (8000, 192), (4096, 0), (1, 8191)):
-        y = qg.cq_fwht_matvec(md["idx"], md["codebook"], md["row_scale"], xt, 512, start, count).cpu().numpy()
+        y = qg.cq_fwht_matvec(md["idx"], md["codebook"], md["row_scale"], xt, group, start, count).cpu().numpy()
         if count:
             assert_close(y, full[start:start + count])
 
 
-def test_cq_constant_index_closed_form():
-    k, g = 512, 512
+@pytest.mark.parametrize("g,k_groups", [(512, 1), (512, 4), (256, 8), (1024, 2)])
+def test_cq_constant_index_closed_form(g, k_groups):
+    """Every index 7: each group's transformed values sum to sqrt(g) times its first
+    element (the Hadamard matrix's column sums are g for column 0 and 0 for the others), so
+    y = scale * C[7] * sqrt(g) * (sum of x[group start]) over the row's groups."""
+    k = g * k_groups
     idx = np.full((4, k), 7, np.uint8)
     from tests._layout import f16_bits, pack_cq
     cb = np.linspace(-0.1, 0.1, 16).astype(np.float32)
@@ -335,7 +340,8 @@ def test_cq_constant_index_closed_form():
     x = datagen.normal_f32(44, 1, k)
     md = dev_w(m)
     y = qg.cq_fwht_matvec(md["idx"], md["codebook"], md["row_scale"], torch.from_numpy(x).to(DEV), g).cpu().numpy()
-    ref = (m["row_scale"].view(np.float16).astype(np.float64) * float(np.float16(cb[7])) * np.sqrt(g) * float(x[0]))
+    heads = float(np.sum(x[::g].astype(np.float64)))
+    ref = m["row_scale"].view(np.float16).astype(np.float64) * float(np.float16(cb[7])) * np.sqrt(g) * heads
     assert_close(y, ref)
 
 
